@@ -1,0 +1,151 @@
+"""Seeded synthetic inputs for the attention path and its oracle.
+
+This module holds no attention arithmetic: it draws the operands, rounds them
+to the storage type and builds the mask descriptions (key lengths, tile mask).
+Both the CUDA path and the oracle consume exactly these arrays, so a parity test
+compares arithmetic only.
+
+Recipe (one numpy ``default_rng`` stream per tensor, spawned from one seed):
+  * Q, K, V, dO ~ N(0, 1), drawn in float32, then rounded to bf16 with
+    round-to-nearest-even (kept exact as float32 for the oracle, and as raw bf16
+    bits for the device);
+  * key-padding lengths: integers uniform on [lo, hi], one per sequence;
+  * block mask over 128x128 tiles: a local band of +-band tiles, the first tile
+    column (global tokens) and a fraction of tiles drawn uniformly without
+    replacement from all tiles.
+The workloads below give the attention shapes of the pages' benchmarks (BERT-large
+and GPT-2 training, long-range contexts, block-sparse attention); no dataset or
+model weights are involved.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+TILE = 128
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns (uint16), round to nearest even; NaN stays NaN."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    nan = np.isnan(x)
+    out = rounded.astype(np.uint16)
+    out[nan] = 0x7FC0
+    return out
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> exactly equal float32 values."""
+    return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bf16 value, returned as float32."""
+    return bf16_bits_to_f32(bf16_bits(x))
+
+
+def _streams(seed: int, n: int):
+    return [np.random.default_rng(s) for s in np.random.SeedSequence(seed).spawn(n)]
+
+
+@dataclass
+class AttentionInputs:
+    """Host copies of one workload's inputs.
+
+    q, k, v, dout: float32 [B, H, N, d] holding bf16-exact values (or true fp32
+    values when dtype == "fp32"); *_bits: the same values as bf16 bit patterns.
+    """
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    dout: np.ndarray
+    dtype: str
+    scale: float
+    causal: bool
+    kv_len: np.ndarray | None
+    block_mask: np.ndarray | None
+    seed: int
+    bits: dict = field(default_factory=dict)
+
+    def device_array(self, name: str) -> np.ndarray:
+        """Array in the device storage type: uint16 bf16 bits, or float32."""
+        a = getattr(self, name)
+        if self.dtype == "fp32":
+            return a
+        if name not in self.bits:
+            self.bits[name] = bf16_bits(a)
+        return self.bits[name]
+
+
+def make_block_mask(n: int, band: int, global_cols: int, frac: float, seed: int,
+                    tile: int = TILE) -> np.ndarray:
+    """uint8 [T, T] tile mask: |i - j| <= band, j < global_cols, plus round(frac*T*T)
+    tiles drawn without replacement from all T*T tiles."""
+    t = (n + tile - 1) // tile
+    i = np.arange(t)[:, None]
+    j = np.arange(t)[None, :]
+    bm = (np.abs(i - j) <= band) | (j < global_cols)
+    rng = _streams(seed, 7)[6]
+    n_rand = int(round(frac * t * t))
+    if n_rand:
+        pick = rng.choice(t * t, size=n_rand, replace=False)
+        bm.reshape(-1)[pick] = True
+    return bm.astype(np.uint8)
+
+
+def make_inputs(B: int, H: int, N: int, d: int, *, seed: int, dtype: str = "bf16",
+                scale: float | None = None, causal: bool = False,
+                kv_len_range: tuple[int, int] | None = None,
+                block_mask: dict | None = None, with_dout: bool = True) -> AttentionInputs:
+    """Draw Q, K, V, dO ~ N(0,1) and the mask description for one workload."""
+    if dtype not in ("bf16", "fp32"):
+        raise ValueError(dtype)
+    rq, rk, rv, rdo, rlen, _rmask, _ = _streams(seed, 7)
+    shape = (B, H, N, d)
+
+    def draw(rng):
+        x = rng.standard_normal(shape, dtype=np.float32)
+        return x if dtype == "fp32" else round_bf16(x)
+
+    q, k, v = draw(rq), draw(rk), draw(rv)
+    dout = draw(rdo) if with_dout else np.zeros(shape, np.float32)
+    kv_len = None
+    if kv_len_range is not None:
+        lo, hi = kv_len_range
+        kv_len = rlen.integers(lo, hi + 1, size=B, dtype=np.int64).astype(np.int32)
+    bm = None
+    if block_mask is not None:
+        bm = make_block_mask(N, seed=seed, **block_mask)
+    return AttentionInputs(q=q, k=k, v=v, dout=dout, dtype=dtype,
+                           scale=(1.0 / math.sqrt(d)) if scale is None else float(scale),
+                           causal=causal, kv_len=kv_len, block_mask=bm, seed=seed)
+
+
+# The five workloads: shapes, masks and scale of the pages' benchmarks.
+WORKLOADS = {
+    "tiny_fp32": dict(B=1, H=1, N=128, d=64, dtype="fp32", scale=1 / 8, causal=False, fwd_only=True),
+    "bert_large_padded": dict(B=16, H=16, N=512, d=64, dtype="bf16", scale=1 / 8, causal=False,
+                              kv_len_range=(256, 512)),
+    "gpt2_causal": dict(B=8, H=12, N=2048, d=64, dtype="bf16", scale=1 / 8, causal=True),
+    "long_causal_16k": dict(B=1, H=32, N=16384, d=128, dtype="bf16", scale=1 / math.sqrt(128), causal=True),
+    "long_causal_64k": dict(B=1, H=32, N=65536, d=128, dtype="bf16", scale=1 / math.sqrt(128), causal=True),
+    "block_sparse_8k": dict(B=4, H=16, N=8192, d=64, dtype="bf16", scale=1 / 8, causal=False,
+                            block_mask=dict(band=4, global_cols=1, frac=0.10)),
+}
+
+WORKLOAD_SEEDS = {
+    "tiny_fp32": 1001, "bert_large_padded": 1002, "gpt2_causal": 1003,
+    "long_causal_16k": 1004, "long_causal_64k": 1004, "block_sparse_8k": 1005,
+}
+
+
+def workload_inputs(name: str, *, seed: int | None = None, **override) -> AttentionInputs:
+    """Inputs of a named workload (optionally with B/H/N overridden for small cases)."""
+    spec = dict(WORKLOADS[name])
+    spec.pop("fwd_only", None)
+    spec.update(override)
+    return make_inputs(seed=WORKLOAD_SEEDS[name] if seed is None else seed, **spec)
