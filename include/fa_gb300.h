@@ -1,0 +1,129 @@
+/*
+ * fa_gb300.h -- C ABI of the exact tiled attention library for one NVIDIA GB300
+ * (sm_103a).
+ *
+ * The library computes exact scaled-dot-product attention with online softmax:
+ *
+ *   S = scale * Q K^T,   P = softmax(S) row by row,   O = P V
+ *
+ * as defined in "FlashAttention: how a memory trick unlocked today's giant AI
+ * models" (khetwal.com), section "The Quadratic Memory Bottleneck" (the three
+ * steps, with the scale written into the score step) and section "The Trick:
+ * Online Softmax" (the softmax formula and the running max / running sum that
+ * let it be computed one key tile at a time).  Following section "Tiling" and
+ * the "FlashAttention (Conceptual)" listing, query tiles of 128 rows stream key
+ * and value tiles of 128 rows through on-chip memory; the N x N matrices S and P
+ * are never written to device memory, so memory use is linear in N.  The
+ * backward pass keeps only the per-row softmax statistic (the log-sum-exp) and
+ * recomputes P from it ("How FlashAttention Eliminates Transformer Memory
+ * Bottlenecks", galileo blog, Innovation #3).  Tiles that a causal or block mask
+ * zeroes out are skipped (same blog, Innovation #5).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors Q, K, V, O, dO, dQ, dK, dV are contiguous [B, H, N, d], d fastest,
+ *    in device memory owned by the caller.  LSE is contiguous [B, H, N] float32.
+ *  - dtype FA_BF16: those tensors hold bfloat16; arithmetic is bf16 x bf16 with
+ *    float32 accumulation, softmax in float32.  dtype FA_FP32 (forward only):
+ *    float32 tensors, float32 arithmetic on CUDA cores.
+ *  - d must be 64 or 128; B, H, N >= 0 (a call with B, H or N equal to 0 does
+ *    nothing and returns FA_OK).  scale must be finite and > 0.
+ *  - LSE[b,h,i] = max_j S_ij + ln(sum_j exp(S_ij - max_j S_ij)) over the keys row
+ *    i sees (natural log, scale included).  A row that sees no key gets O = 0,
+ *    LSE = -inf and dQ = 0.
+ *  - causal != 0: query i sees key j only if j <= i.
+ *  - kv_len (device, int32 [B], may be NULL): keys j >= kv_len[b] are masked for
+ *    every query of sequence b (key padding).  Values are clamped to [0, N].
+ *  - block_mask (device, uint8 [T, T] row-major with T = ceil(N / 128), may be
+ *    NULL): query tile i sees key tile j only if block_mask[i*T + j] != 0.  One
+ *    mask is shared by all B*H heads; masked tiles are skipped, kept tiles are
+ *    computed in full.  The three masks combine by AND.
+ *  - Pointers to the [B,H,N,d] tensors and to workspaces must be 16-byte aligned
+ *    (the kernels move tiles with TMA); lse must be 4-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  All calls are
+ *    asynchronous with respect to the host; they enqueue kernels on `stream` and
+ *    return.  The library allocates no device memory.
+ *
+ * Errors: argument checks run on the host before anything is enqueued; a failed
+ * check returns FA_ERR_INVALID_ARG or FA_ERR_UNSUPPORTED and launches nothing.
+ * A CUDA error while encoding descriptors or launching returns FA_ERR_CUDA.
+ * Every device-side wait is bounded; a wait that gives up records FA_ERR_TIMEOUT
+ * in a device status word that fa_get_device_status() reads.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, negative size, bad scale, small workspace */
+  FA_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, unknown dtype, fp32 backward */
+  FA_ERR_CUDA = 3,         /* CUDA runtime/driver error on the host side */
+  FA_ERR_TIMEOUT = 4       /* a device-side wait gave up (reported by fa_get_device_status) */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_FP32 = 1 } fa_dtype;
+
+/* Forward pass: O = softmax(scale * Q K^T) V and LSE, as defined above.
+ * q, k, v: inputs [B,H,N,d]; o: output [B,H,N,d]; lse: output [B,H,N] float32.
+ * One kernel launch.  The tiles of S live only in tensor memory and registers. */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, float scale, int causal,
+                 const uint8_t* block_mask, const int32_t* kv_len, int dtype, void* stream);
+
+/* Bytes of device workspace fa_bwd needs: D = rowsum(dO * O) (float32 [B,H,N])
+ * and the float32 dQ accumulator [B,H,N,d], each 256-byte aligned.  Linear in N. */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/* Backward pass (bf16 only): given the forward's inputs, its outputs O and LSE and
+ * the output gradient dO, writes dQ, dK, dV [B,H,N,d] for L = sum(O * dO):
+ *   dP = dO V^T,  D_i = sum_c dO_ic O_ic,  dS = P * (dP - D),
+ *   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO,
+ * with P recomputed from Q, K and LSE.  The pages give no backward formulas; these
+ * are the chain rule applied to the forward definition.  Keys that no query sees
+ * get dK = dV = 0.  workspace: caller-owned device memory of at least
+ * fa_bwd_workspace_size() bytes (contents on entry are ignored).
+ * Equivalent to fa_bwd_preprocess + fa_bwd_main + fa_bwd_postprocess. */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                 int B, int H, int N, int d, float scale, int causal,
+                 const uint8_t* block_mask, const int32_t* kv_len, int dtype, void* stream);
+
+/* Backward stage 1: D = rowsum(dO * O) into the workspace and zero the float32 dQ
+ * accumulator.  Memory-bound.  o, dout: bf16 [B,H,N,d]. */
+fa_status fa_bwd_preprocess(const void* o, const void* dout, void* workspace, size_t workspace_bytes,
+                            int B, int H, int N, int d, void* stream);
+
+/* Backward stage 2: one CTA per 128-key tile recomputes P for every query tile that
+ * sees it and accumulates dK, dV (written as bf16) and dQ (float32 atomics into the
+ * workspace accumulator).  Needs stage 1 to have run on the same workspace. */
+fa_status fa_bwd_main(const void* q, const void* k, const void* v, const float* lse, const void* dout,
+                      void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                      int B, int H, int N, int d, float scale, int causal,
+                      const uint8_t* block_mask, const int32_t* kv_len, void* stream);
+
+/* Backward stage 3: dQ (bf16) = the float32 accumulator in the workspace. */
+fa_status fa_bwd_postprocess(void* dq, const void* workspace, size_t workspace_bytes,
+                             int B, int H, int N, int d, void* stream);
+
+/* Synchronises `stream`, then returns and clears the device status word:
+ * FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if the synchronisation itself failed. */
+fa_status fa_get_device_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

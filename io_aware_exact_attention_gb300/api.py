@@ -1,0 +1,131 @@
+"""Python binding of the C ABI (include/fa_gb300.h).
+
+Argument marshalling only: every step of the attention path runs in the CUDA
+library.  Tensors are torch CUDA tensors (torch supplies device memory and the
+current stream); the C entry points get raw pointers and sizes.  The functions
+with C names take caller-allocated outputs; ``attention_forward`` /
+``attention_backward`` allocate outputs and workspace with torch first.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+_DTYPES = {torch.bfloat16: _lib.FA_BF16, torch.float32: _lib.FA_FP32}
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {_lib.status_string(code)}")
+
+
+def _check(code: int, where: str):
+    if code != _lib.FA_OK:
+        raise FaError(code, where)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _shape(q):
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    return tuple(int(x) for x in q.shape)
+
+
+def _same(ref, *ts):
+    for t in ts:
+        if t is not None and (t.shape != ref.shape or t.dtype != ref.dtype or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous with equal shape and dtype")
+
+
+def fa_fwd(q, k, v, o, lse, scale, causal=False, block_mask=None, kv_len=None, stream=None):
+    """O, LSE <- attention(Q, K, V); all [B,H,N,d] contiguous CUDA tensors, lse [B,H,N] float32."""
+    B, H, N, d = _shape(q)
+    _same(q, k, v, o)
+    if not q.is_contiguous() or lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
+        raise ValueError("bad q or lse")
+    dtype = _DTYPES.get(q.dtype)
+    if dtype is None:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    code = _lib.load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
+                              int(bool(causal)), _ptr(block_mask), _ptr(kv_len), dtype, _stream(stream))
+    _check(code, "fa_fwd")
+
+
+def fa_bwd_workspace_size(B, H, N, d) -> int:
+    return int(_lib.load().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, scale, causal=False, block_mask=None, kv_len=None,
+           stream=None):
+    """dQ, dK, dV <- backward of attention for upstream gradient dO (bf16)."""
+    B, H, N, d = _shape(q)
+    _same(q, k, v, o, dout, dq, dk, dv)
+    if q.dtype != torch.bfloat16:
+        raise ValueError("backward takes bf16 tensors")
+    code = _lib.load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                              _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, N, d,
+                              float(scale), int(bool(causal)), _ptr(block_mask), _ptr(kv_len), _lib.FA_BF16,
+                              _stream(stream))
+    _check(code, "fa_bwd")
+
+
+def fa_bwd_preprocess(o, dout, workspace, stream=None):
+    B, H, N, d = _shape(o)
+    code = _lib.load().fa_bwd_preprocess(_ptr(o), _ptr(dout), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), B, H, N, d, _stream(stream))
+    _check(code, "fa_bwd_preprocess")
+
+
+def fa_bwd_main(q, k, v, lse, dout, dk, dv, workspace, scale, causal=False, block_mask=None, kv_len=None,
+                stream=None):
+    B, H, N, d = _shape(q)
+    code = _lib.load().fa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(dout), _ptr(dk), _ptr(dv),
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, N, d,
+                                   float(scale), int(bool(causal)), _ptr(block_mask), _ptr(kv_len), _stream(stream))
+    _check(code, "fa_bwd_main")
+
+
+def fa_bwd_postprocess(dq, workspace, stream=None):
+    B, H, N, d = _shape(dq)
+    code = _lib.load().fa_bwd_postprocess(_ptr(dq), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          B, H, N, d, _stream(stream))
+    _check(code, "fa_bwd_postprocess")
+
+
+def fa_get_device_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the device status word (0 = FA_OK)."""
+    return int(_lib.load().fa_get_device_status(_stream(stream)))
+
+
+def attention_forward(q, k, v, scale, causal=False, block_mask=None, kv_len=None, stream=None):
+    """Allocate O and LSE with torch and run fa_fwd.  Returns (o, lse)."""
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], device=q.device, dtype=torch.float32)
+    fa_fwd(q, k, v, o, lse, scale, causal, block_mask, kv_len, stream)
+    return o, lse
+
+
+def new_workspace(q):
+    B, H, N, d = _shape(q)
+    nbytes = fa_bwd_workspace_size(B, H, N, d)
+    return torch.empty(max(nbytes, 16), device=q.device, dtype=torch.uint8)
+
+
+def attention_backward(q, k, v, o, lse, dout, scale, causal=False, block_mask=None, kv_len=None, workspace=None,
+                       stream=None):
+    """Allocate dQ, dK, dV (and the workspace if none is given) and run fa_bwd."""
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = new_workspace(q) if workspace is None else workspace
+    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, ws, scale, causal, block_mask, kv_len, stream)
+    return dq, dk, dv

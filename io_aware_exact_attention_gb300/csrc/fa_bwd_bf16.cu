@@ -1,0 +1,473 @@
+// Backward pass, bf16 in / fp32 accumulate.
+//
+// The pages keep only the per-row softmax statistics after the forward pass and
+// recompute what back-propagation needs ("How FlashAttention Eliminates
+// Transformer Memory Bottlenecks", galileo blog, Innovation #3).  They give no
+// formulas; these kernels apply the chain rule to S = scale Q K^T, P = softmax(S),
+// O = P V with L = sum(O * dO):
+//   P  = exp(S - LSE)            (recomputed, one exp per score)
+//   dV = P^T dO,   dP = dO V^T,  D = rowsum(dO * O),  dS = P * (dP - D)
+//   dK = scale dS^T Q,           dQ = scale dS K
+// Three launches:
+//   1. preprocess: D per query row, and the float32 dQ accumulator set to zero;
+//   2. main: one CTA per 128-row key tile K_j, V_j (kept in shared memory) loops
+//      over the query tiles Q_i that see it.  Five tcgen05 MMAs per tile pair:
+//        S = Q_i K_j^T and dP = dO_i V_j^T (TMEM, lanes = query rows),
+//        dV += P^T dO_i and dK += dS^T Q_i (TMEM accumulators, lanes = key rows),
+//        dQ_i = dS K_j (TMEM, added to the float32 accumulator with atomics).
+//      P and dS are written once to shared memory as bf16 in a 128-byte-swizzled
+//      [query][key] layout; the same bytes serve as a K-major operand (dQ) and,
+//      read M-major, as the transposed operand (dV, dK).
+//   3. postprocess: dQ (bf16) from the float32 accumulator.
+#include "fa_internal.h"
+#include "fa_tiles.cuh"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBwdThreads = 192;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+template <int D>
+struct BwdLayout {
+  static constexpr int kQStages = D == 64 ? 2 : 1;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kSubBytes = kTile * 64 * 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kQ = kV + kTileBytes;
+  static constexpr int kDO = kQ + kQStages * kTileBytes;
+  static constexpr int kP = kDO + kQStages * kTileBytes;
+  static constexpr int kDS = kP + kTile * kTile * 2;
+  static constexpr int kEnd = kDS + kTile * kTile * 2;
+  static constexpr int kSmemBytes = kEnd + 1024;
+  // TMEM columns
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColDP = 128;
+  static constexpr uint32_t kColDV = 256;
+  static constexpr uint32_t kColDK = 256 + D;
+  static constexpr bool kDqAliasesS = (256 + 3 * D) > 512;
+  static constexpr uint32_t kColDQ = kDqAliasesS ? 0u : static_cast<uint32_t>(256 + 2 * D);
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+template <int D>
+struct BwdBarriers {
+  uint64_t kv_full;
+  uint64_t qdo_full[BwdLayout<D>::kQStages];
+  uint64_t qdo_empty[BwdLayout<D>::kQStages];
+  uint64_t s_full, dp_full, p_full, dv_done, ds_full, dkdq_done, dq_free, drain;
+};
+
+__device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000); }
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                    const float* __restrict__ lse, const float* __restrict__ dsum, float* __restrict__ dq_acc,
+                    const AttnArgs a) {
+  using L = BwdLayout<D>;
+  constexpr int QS = L::kQStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) BwdBarriers<D> bar;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int T = a.n_tiles;
+  const int head = blockIdx.x / T;
+  const int kt = blockIdx.x % T;  // key tile owned by this CTA
+  const int b = head / a.H;
+  const int kv_len = clamp_kv_len(a.kv_len, b, a.N);
+  const int qt_first = a.causal ? kt : 0;
+  const WaitCtx wc{&abort_flag, a.status};
+
+  uint8_t* smK = smem + L::kK;
+  uint8_t* smV = smem + L::kV;
+  uint8_t* smQ = smem + L::kQ;
+  uint8_t* smDO = smem + L::kDO;
+  uint8_t* smP = smem + L::kP;
+  uint8_t* smDS = smem + L::kDS;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar.kv_full, 1);
+    for (int s = 0; s < QS; ++s) {
+      mbar_init(&bar.qdo_full[s], 1);
+      mbar_init(&bar.qdo_empty[s], 1);
+    }
+    mbar_init(&bar.s_full, 1);
+    mbar_init(&bar.dp_full, 1);
+    mbar_init(&bar.p_full, 128);
+    mbar_init(&bar.dv_done, 1);
+    mbar_init(&bar.ds_full, 128);
+    mbar_init(&bar.dkdq_done, 1);
+    mbar_init(&bar.dq_free, 128);
+    mbar_init(&bar.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_s, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      const int first = next_query_tile(qt_first, kt, kv_len, a.causal, a.block_mask, T);
+      if (first < T) {
+        mbar_arrive_expect_tx(&bar.kv_full, 2 * L::kTileBytes);
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_3d(smK + h * L::kSubBytes, &tm_k, &bar.kv_full, h * 64, kt * kTile, head);
+          tma_load_3d(smV + h * L::kSubBytes, &tm_v, &bar.kv_full, h * 64, kt * kTile, head);
+        }
+      }
+      for (int qt = first; qt < T; qt = next_query_tile(qt + 1, kt, kv_len, a.causal, a.block_mask, T), ++it) {
+        const int s = it % QS;
+        if (it >= QS && !(ok = mbar_wait(&bar.qdo_empty[s], ((it / QS) - 1) & 1, wc))) break;
+        mbar_arrive_expect_tx(&bar.qdo_full[s], 2 * L::kTileBytes);
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_3d(smQ + s * L::kTileBytes + h * L::kSubBytes, &tm_q, &bar.qdo_full[s], h * 64, qt * kTile, head);
+          tma_load_3d(smDO + s * L::kTileBytes + h * L::kSubBytes, &tm_do, &bar.qdo_full[s], h * 64, qt * kTile,
+                      head);
+        }
+      }
+      if (!ok) {
+        if (first < T) mbar_drain(&bar.kv_full, 0, 100000000ull);
+        for (int j = (it > QS ? it - QS : 0); j < it; ++j) mbar_drain(&bar.qdo_full[j % QS], (j / QS) & 1, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);   // S, dP
+      constexpr uint32_t id_t = idesc_bf16_f32(128, D, true, true);       // dV, dK (transposed A)
+      constexpr uint32_t id_q = idesc_bf16_f32(128, D, false, true);      // dQ
+      const uint32_t k0 = smem_u32(smK), v0 = smem_u32(smV), p0 = smem_u32(smP), ds0 = smem_u32(smDS);
+      bool ok = true;
+      int it = 0;
+      const int first = next_query_tile(qt_first, kt, kv_len, a.causal, a.block_mask, T);
+      if (first < T) ok = mbar_wait(&bar.kv_full, 0, wc);
+      if (ok) {
+        for (int qt = first; qt < T; qt = next_query_tile(qt + 1, kt, kv_len, a.causal, a.block_mask, T), ++it) {
+          const int s = it % QS;
+          const uint32_t q0 = smem_u32(smQ + s * L::kTileBytes), do0 = smem_u32(smDO + s * L::kTileBytes);
+          if (!(ok = mbar_wait(&bar.qdo_full[s], (it / QS) & 1, wc))) break;
+          if (L::kDqAliasesS && it >= 1 && !(ok = mbar_wait(&bar.dq_free, (it - 1) & 1, wc))) break;
+          tc_fence_after();
+          // S = Q_i K_j^T and dP = dO_i V_j^T
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
+            mma_bf16_ss(tmem + L::kColS, sdesc_sw128(q0 + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024), id_s,
+                        k > 0 ? 1u : 0u);
+          }
+          mma_commit(&bar.s_full);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
+            mma_bf16_ss(tmem + L::kColDP, sdesc_sw128(do0 + off, 16, 1024), sdesc_sw128(v0 + off, 16, 1024), id_s,
+                        k > 0 ? 1u : 0u);
+          }
+          mma_commit(&bar.dp_full);
+          // dV += P^T dO_i
+          if (!(ok = mbar_wait(&bar.p_full, it & 1, wc))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k)
+            mma_bf16_ss(tmem + L::kColDV, sdesc_sw128(p0 + k * 2048, L::kSubBytes, 1024),
+                        sdesc_sw128(do0 + k * 2048, L::kSubBytes, 1024), id_t, (it > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bar.dv_done);
+          // dK += dS^T Q_i ; dQ_i = dS K_j
+          if (!(ok = mbar_wait(&bar.ds_full, it & 1, wc))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k)
+            mma_bf16_ss(tmem + L::kColDK, sdesc_sw128(ds0 + k * 2048, L::kSubBytes, 1024),
+                        sdesc_sw128(q0 + k * 2048, L::kSubBytes, 1024), id_t, (it > 0 || k > 0) ? 1u : 0u);
+          if (!L::kDqAliasesS && it >= 1 && !(ok = mbar_wait(&bar.dq_free, (it - 1) & 1, wc))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k)
+            mma_bf16_ss(tmem + L::kColDQ, sdesc_sw128(ds0 + (k / 4) * L::kSubBytes + (k % 4) * 32, 16, 1024),
+                        sdesc_sw128(k0 + k * 2048, L::kSubBytes, 1024), id_q, k > 0 ? 1u : 0u);
+          mma_commit(&bar.dkdq_done);
+          mma_commit(&bar.qdo_empty[s]);
+        }
+      }
+      if (!ok) {
+        mma_commit(&bar.drain);
+        mbar_drain(&bar.drain, 0, 100000000ull);
+      }
+    }
+  } else {
+    // ---------------------------------------------- P, dS, dQ and the epilogue
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // query row (for S, dP, dQ) or key row (for dK, dV) inside the tile
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const float sl2 = a.scale_log2;
+    const int key0 = kt * kTile;
+    bool ok = true;
+    int it = 0;
+    const int first = next_query_tile(qt_first, kt, kv_len, a.causal, a.block_mask, T);
+    for (int qt = first; qt < T; qt = next_query_tile(qt + 1, kt, kv_len, a.causal, a.block_mask, T), ++it) {
+      const int q_row = qt * kTile + r;
+      const bool row_ok = q_row < a.N;
+      const size_t row_idx = static_cast<size_t>(head) * a.N + q_row;
+      float lse_r = row_ok ? lse[row_idx] : pos_inf();
+      if (lse_r == -pos_inf()) lse_r = pos_inf();  // a row that sees no key contributes nothing
+      const float lse2 = lse_r * kLog2e;
+      const float d_r = row_ok ? dsum[row_idx] : 0.f;
+      const bool need_mask = (key0 + kTile > kv_len) || (a.causal && kt == qt);
+      const int lim = a.causal ? min(kv_len, q_row + 1) : kv_len;  // keys [key0, lim) visible
+
+      ok = mbar_wait(&bar.s_full, it & 1, wc);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t pk[kTile / 2];
+#pragma unroll
+      for (int c0 = 0; c0 < kTile; c0 += 32) {
+        uint32_t t[32];
+        tmem_ld32(tmem + lane_off + L::kColS + c0, t);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float p0 = ex2(fmaf(__uint_as_float(t[i]), sl2, -lse2));
+          float p1 = ex2(fmaf(__uint_as_float(t[i + 1]), sl2, -lse2));
+          if (need_mask) {
+            if (key0 + c0 + i >= lim) p0 = 0.f;
+            if (key0 + c0 + i + 1 >= lim) p1 = 0.f;
+          }
+          pk[(c0 + i) / 2] = pack_bf16x2(p0, p1);
+        }
+      }
+      if (it >= 1) {
+        ok = mbar_wait(&bar.dv_done, (it - 1) & 1, wc);  // P_{i-1} no longer read by the dV MMA
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      }
+      const uint32_t prow = smem_u32(smP);
+#pragma unroll
+      for (int g = 0; g < kTile / 8; ++g)
+        st_shared_v4(prow + (g / 8) * L::kSubBytes + sw128_offset(r, g % 8), pk[4 * g], pk[4 * g + 1],
+                     pk[4 * g + 2], pk[4 * g + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar.p_full);
+
+      ok = mbar_wait(&bar.dp_full, it & 1, wc);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      // dS_{i-1} is free: the dK/dQ MMAs that read it completed (waited at the end of the previous tile),
+      // so each 32-column chunk of dS goes to shared memory as soon as it is formed.
+      const uint32_t dsrow = smem_u32(smDS);
+#pragma unroll
+      for (int c0 = 0; c0 < kTile; c0 += 32) {
+        uint32_t t[32];
+        tmem_ld32(tmem + lane_off + L::kColDP + c0, t);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const uint32_t pp = pk[(c0 + i) / 2];
+          const float ds0 = bf16lo(pp) * (__uint_as_float(t[i]) - d_r);
+          const float ds1 = bf16hi(pp) * (__uint_as_float(t[i + 1]) - d_r);
+          w[i / 2] = pack_bf16x2(ds0, ds1);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int g = c0 / 8 + q;
+          st_shared_v4(dsrow + (g / 8) * L::kSubBytes + sw128_offset(r, g % 8), w[4 * q], w[4 * q + 1],
+                       w[4 * q + 2], w[4 * q + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar.ds_full);
+
+      // dQ_i partial: scale * dS K_j, added into the float32 accumulator
+      ok = mbar_wait(&bar.dkdq_done, it & 1, wc);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      float* dq_row = dq_acc + row_idx * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t t[32];
+        tmem_ld32(tmem + lane_off + L::kColDQ + c0, t);
+        if (row_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            float4 v4 = make_float4(__uint_as_float(t[i]) * a.scale, __uint_as_float(t[i + 1]) * a.scale,
+                                    __uint_as_float(t[i + 2]) * a.scale, __uint_as_float(t[i + 3]) * a.scale);
+            atomicAdd(reinterpret_cast<float4*>(dq_row + c0 + i), v4);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar.dq_free);
+    }
+
+    // epilogue: dV_j and scale * dK_j as bf16 through shared memory and TMA.
+    const bool have = ok && it > 0;
+    // all MMAs completed: the last dkdq_done was waited above, and it follows every earlier MMA
+    tc_fence_after();
+    const uint32_t stage_v = smem_u32(smQ), stage_k = smem_u32(smDO);
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      uint32_t tv[32], tk[32];
+      if (have) {
+        tmem_ld32(tmem + lane_off + L::kColDV + c0, tv);
+        tmem_ld32(tmem + lane_off + L::kColDK + c0, tk);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) tv[i] = tk[i] = 0u;
+      }
+      uint32_t wv[16], wk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        wv[i] = pack_bf16x2(__uint_as_float(tv[2 * i]), __uint_as_float(tv[2 * i + 1]));
+        wk[i] = pack_bf16x2(__uint_as_float(tk[2 * i]) * a.scale, __uint_as_float(tk[2 * i + 1]) * a.scale);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t off = (c0 / 64) * L::kSubBytes + sw128_offset(r, ((c0 % 64) / 8) + q);
+        st_shared_v4(stage_v + off, wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
+        st_shared_v4(stage_k + off, wk[4 * q], wk[4 * q + 1], wk[4 * q + 2], wk[4 * q + 3]);
+      }
+    }
+    fence_proxy_async_smem();
+    named_barrier(1, 128);
+    if (warp == 2 && lane == 0) {
+      for (int h = 0; h < D / 64; ++h) {
+        tma_store_3d(&tm_dv, smQ + h * L::kSubBytes, h * 64, kt * kTile, head);
+        tma_store_3d(&tm_dk, smDO + h * L::kSubBytes, h * 64, kt * kTile, head);
+      }
+      tma_store_commit();
+      tma_store_wait_all();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+// D_i = sum_c dO_ic O_ic (float32) for every row, and dq_acc = 0.
+// Eight bf16 per lane; D / 8 lanes share a row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
+                                                             float* __restrict__ dsum, float4* __restrict__ dq_acc,
+                                                             long long rows) {
+  constexpr int kLanesPerRow = D / 8;
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+  // rows handled in groups so every lane of a warp stays active for the shuffles
+  const long long row_slots = (rows * kLanesPerRow + 31) / 32 * 32;
+  for (long long e = tid; e < row_slots; e += nthreads) {
+    const long long row = e / kLanesPerRow;
+    const int part = static_cast<int>(e % kLanesPerRow);
+    float acc = 0.f;
+    if (row < rows) {
+      const uint4 x = o[row * kLanesPerRow + part];
+      const uint4 y = dout[row * kLanesPerRow + part];
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc = fmaf(bf16lo(xs[i]), bf16lo(ys[i]), acc);
+        acc = fmaf(bf16hi(xs[i]), bf16hi(ys[i]), acc);
+      }
+    }
+#pragma unroll
+    for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows && part == 0) dsum[row] = acc;
+  }
+  const long long n4 = rows * D / 4;
+  for (long long e = tid; e < n4; e += nthreads) dq_acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// dq (bf16) = dq_acc (float32), eight elements per thread.
+__global__ void __launch_bounds__(256) bwd_postprocess_kernel(const float4* __restrict__ dq_acc,
+                                                              uint4* __restrict__ dq, long long n8) {
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long e = tid; e < n8; e += nthreads) {
+    const float4 x = dq_acc[2 * e], y = dq_acc[2 * e + 1];
+    dq[e] = make_uint4(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w), pack_bf16x2(y.x, y.y), pack_bf16x2(y.z, y.w));
+  }
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n = 152;
+  }
+  return n;
+}
+
+unsigned grid_for(long long work, int per_block) {
+  long long blocks = (work + per_block - 1) / per_block;
+  const long long cap = static_cast<long long>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  return static_cast<unsigned>(blocks < 1 ? 1 : blocks);
+}
+
+template <int D>
+cudaError_t launch_bwd_main_d(const BwdMaps& m, const float* lse, const float* dsum, float* dq_acc, const AttnArgs& a,
+                              cudaStream_t stream) {
+  using L = BwdLayout<D>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const long long grid = static_cast<long long>(a.n_tiles) * a.B * a.H;
+  bwd_main_kernel<D><<<static_cast<unsigned>(grid), kBwdThreads, L::kSmemBytes, stream>>>(
+      m.q, m.k, m.v, m.dout, m.dk, m.dv, lse, dsum, dq_acc, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* dsum, float* dq_acc, const AttnArgs& a,
+                                  cudaStream_t stream) {
+  const long long rows = static_cast<long long>(a.B) * a.H * a.N;
+  const unsigned grid = grid_for(rows * (a.d / 8), 256);
+  if (a.d == 64)
+    bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout),
+                                                        dsum, reinterpret_cast<float4*>(dq_acc), rows);
+  else
+    bwd_preprocess_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout),
+                                                         dsum, reinterpret_cast<float4*>(dq_acc), rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main_bf16(const BwdMaps& maps, const float* lse, const float* dsum, float* dq_acc,
+                                 const AttnArgs& a, cudaStream_t stream) {
+  return a.d == 64 ? launch_bwd_main_d<64>(maps, lse, dsum, dq_acc, a, stream)
+                   : launch_bwd_main_d<128>(maps, lse, dsum, dq_acc, a, stream);
+}
+
+cudaError_t launch_bwd_postprocess(const float* dq_acc, void* dq, const AttnArgs& a, cudaStream_t stream) {
+  const long long n8 = static_cast<long long>(a.B) * a.H * a.N * a.d / 8;
+  bwd_postprocess_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
+                                                                static_cast<uint4*>(dq), n8);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,47 @@
+// Internal interface between the host entry points (fa_api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+constexpr int kTile = 128;  // query and key tile edge (rows)
+
+// Arguments common to the attention kernels (forward and backward).
+struct AttnArgs {
+  int B, H, N, d;
+  int n_tiles;                // ceil(N / 128)
+  float scale;                // softmax scale
+  float scale_log2;           // scale * log2(e): scores go straight to the exp2 domain
+  int causal;
+  const uint8_t* block_mask;  // [n_tiles, n_tiles] or null
+  const int32_t* kv_len;      // [B] or null
+  unsigned int* status;       // device status word
+};
+
+// Tensor maps for [B*H, N, d] bf16 tensors, boxes of 64 x 128 with 128-byte swizzle.
+struct FwdMaps {
+  CUtensorMap q, k, v, o;
+};
+
+struct BwdMaps {
+  CUtensorMap q, k, v, dout, dk, dv;
+};
+
+cudaError_t launch_fwd_bf16(const FwdMaps& maps, float* lse, const AttnArgs& a, cudaStream_t stream);
+
+cudaError_t launch_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse,
+                            const AttnArgs& a, cudaStream_t stream);
+
+cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* dsum, float* dq_acc,
+                                  const AttnArgs& a, cudaStream_t stream);
+
+cudaError_t launch_bwd_main_bf16(const BwdMaps& maps, const float* lse, const float* dsum, float* dq_acc,
+                                 const AttnArgs& a, cudaStream_t stream);
+
+cudaError_t launch_bwd_postprocess(const float* dq_acc, void* dq, const AttnArgs& a, cudaStream_t stream);
+
+}  // namespace fa
