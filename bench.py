@@ -1,0 +1,470 @@
+"""Benchmark: exact tiled attention forward + backward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one pass of the whole attention path over one batch of the workload:
+fa_fwd (one kernel) then fa_bwd's three stages (preprocess, main, postprocess),
+inputs resident in HBM.  Timed with CUDA events on the launching stream, L2
+flushed (512 MiB written) between timed steps, max over ranks.  Prints one JSON
+line (rank 0).
+
+FLOP convention: forward 4*B*H*N^2*d (halved when causal), backward 2.5x forward;
+`value` is forward+backward TFLOP/s.  The roofline object reports the dominant
+kernel against the measured dense bf16 peak, with achieved FLOPs counted over the
+128x128 tile pairs the kernel actually visits (4*128*128*d per pair forward,
+10*128*128*d backward).
+
+--impl reference times the fp64 CPU oracle on the host cores instead (one head of
+the workload per step), as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from io_aware_exact_attention_gb300 import inputs  # noqa: E402
+
+METRIC = "attention TFLOP/s fwd & fwd+bwd bf16 on 1 GB300; % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+FLUSH_BYTES = 512 << 20
+TILE = 128
+EXTRA_WORKLOAD = "long_causal_16k"
+
+
+# ------------------------------------------------------------------ host logic
+
+def formula_fwd_flops(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def visited_tile_pairs(N, causal, kv_len, block_mask, B, H):
+    """Number of (query tile, key tile) pairs the kernels visit, summed over heads."""
+    T = (N + TILE - 1) // TILE
+    qt = np.arange(T)[:, None]
+    kt = np.arange(T)[None, :]
+    total = 0
+    for b in range(B):
+        vis = np.ones((T, T), bool)
+        kl = N if kv_len is None else int(min(max(kv_len[b], 0), N))
+        vis &= kt * TILE < kl
+        if causal:
+            vis &= kt <= qt
+        if block_mask is not None:
+            vis &= np.asarray(block_mask).astype(bool)
+        total += int(vis.sum()) * H
+    return total
+
+
+def algorithmic_flops(pairs, d):
+    return {"fwd": pairs * 4.0 * TILE * TILE * d, "bwd": pairs * 10.0 * TILE * TILE * d}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        p = json.load(open(path))
+        return {"bf16_tflops": float(p["bf16_tflops"]), "bf16_tflops_sustained": float(p["bf16_tflops_sustained"]),
+                "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_digest(kernel):
+    import hashlib
+    src = {"bwd_main": "fa_bwd_bf16.cu", "fwd": "fa_fwd_bf16.cu"}.get(kernel)
+    if src is None:
+        return None
+    h = hashlib.sha256()
+    for name in (src, "sm103_ptx.cuh", "fa_tiles.cuh"):
+        h.update(open(os.path.join(ROOT, "io_aware_exact_attention_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source; None otherwise."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    pat = re.compile(r"^\|\s*" + re.escape(kernel) + r"\s*\|\s*" + re.escape(workload) +
+                     r"\s*\|\s*([0-9.eE+]+)\s*\|\s*([0-9a-f]+)\s*\|")
+    digest = kernel_source_digest(kernel)
+    for line in open(path):
+        m = pat.match(line)
+        if m and m.group(2) == digest:
+            return float(m.group(1))
+    return None
+
+
+def reduce_max_over_ranks(x, dist=None):
+    """Max of a float over ranks (identity without a process group)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_line(per_rank_flops, world, max_ms_step, steps):
+    """Whole-job throughput: units of all ranks over the slowest rank's time."""
+    total_flops = per_rank_flops * world
+    return total_flops / (max_ms_step * 1e-3) / 1e12
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu_index), "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        return parse_clock_lines(getattr(self, "lines", []))
+
+
+def parse_clock_lines(lines):
+    sm, mx, reasons = [], None, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for ln in lines:
+        f = [x.strip() for x in ln.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            sm.append(float(f[1]))
+            mx = float(f[2])
+        except ValueError:
+            continue
+        for name, val in zip(names, f[5:9]):
+            if val.lower().startswith("active"):
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def device_inputs(inp, torch):
+    def dev(name):
+        a = inp.device_array(name)
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    t = {n: dev(n) for n in ("q", "k", "v", "dout")}
+    t["block_mask"] = torch.from_numpy(inp.block_mask).cuda() if inp.block_mask is not None else None
+    t["kv_len"] = torch.from_numpy(inp.kv_len).cuda() if inp.kv_len is not None else None
+    return t
+
+
+def time_workload(name, steps, warmup, torch, fa, flush, dist=None, sampler=None, override=None):
+    """Run `steps` timed fwd+bwd steps on one workload; per-stage CUDA-event times."""
+    spec = inputs.WORKLOADS[name]
+    inp = inputs.workload_inputs(name, **(override or {}))
+    B, H, N, d = inp.q.shape
+    t = device_inputs(inp, torch)
+    q, k, v, do, bm, kl = t["q"], t["k"], t["v"], t["dout"], t["block_mask"], t["kv_len"]
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device="cuda", dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = fa.new_workspace(q)
+    stream = torch.cuda.current_stream()
+    scale, causal = inp.scale, spec["causal"]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fa_fwd(q, k, v, o, lse, scale, causal, bm, kl, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        fa.fa_bwd_preprocess(o, do, ws, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        fa.fa_bwd_main(q, k, v, lse, do, dk, dv, ws, scale, causal, bm, kl, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        fa.fa_bwd_postprocess(dq, ws, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    if dist is not None and dist.is_initialized():
+        dist.barrier()
+    torch.cuda.synchronize()
+    ctx = sampler if sampler is not None else _Null()
+    with ctx:
+        t0 = time.perf_counter()
+        for i in range(steps):
+            flush.zero_()
+            step(events[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if dist is not None and dist.is_initialized():
+        dist.barrier()
+    if fa.fa_get_device_status() != 0:
+        raise RuntimeError("device status reports a timed-out wait")
+    stage = {"fwd": 0.0, "bwd_preprocess": 0.0, "bwd_main": 0.0, "bwd_postprocess": 0.0}
+    keys = list(stage)
+    for ev in events:
+        for j, key in enumerate(keys):
+            stage[key] += ev[j].elapsed_time(ev[j + 1])
+    ms = {k2: v2 / steps for k2, v2 in stage.items()}
+    ms["step"] = sum(ms.values())
+    ms["wall_s"] = wall
+    pairs = visited_tile_pairs(N, causal, inp.kv_len, inp.block_mask, B, H)
+    return inp, ms, pairs, (q, k, v, do, bm, kl)
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def e2e_throughput(inp, steps, torch, fa):
+    """Same fwd+bwd through the public API from pinned host buffers; copies in the timed region."""
+    B, H, N, d = inp.q.shape
+    spec_causal = inp.causal
+    host = {n: torch.from_numpy(np.ascontiguousarray(inp.device_array(n)).view(np.int16)).view(torch.bfloat16)
+            .pin_memory() for n in ("q", "k", "v", "dout")}
+    host_kl = torch.from_numpy(inp.kv_len).pin_memory() if inp.kv_len is not None else None
+    host_bm = torch.from_numpy(inp.block_mask).pin_memory() if inp.block_mask is not None else None
+    dev = {n: torch.empty(host[n].shape, dtype=torch.bfloat16, device="cuda") for n in host}
+    kl = torch.empty_like(host_kl, device="cuda") if host_kl is not None else None
+    bm = torch.empty_like(host_bm, device="cuda") if host_bm is not None else None
+    outs_host = {n: torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory() for n in ("o", "dq", "dk", "dv")}
+    lse_host = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    ws = fa.new_workspace(dev["q"])
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d += (host_kl.numel() * 4 if host_kl is not None else 0) + (host_bm.numel() if host_bm is not None else 0)
+    d2h = sum(t.numel() * t.element_size() for t in outs_host.values()) + lse_host.numel() * 4
+
+    def one():
+        for n in host:
+            dev[n].copy_(host[n], non_blocking=True)
+        if kl is not None:
+            kl.copy_(host_kl, non_blocking=True)
+        if bm is not None:
+            bm.copy_(host_bm, non_blocking=True)
+        o, lse = fa.attention_forward(dev["q"], dev["k"], dev["v"], inp.scale, spec_causal, bm, kl, stream)
+        dq, dk, dv = fa.attention_backward(dev["q"], dev["k"], dev["v"], o, lse, dev["dout"], inp.scale, spec_causal,
+                                           bm, kl, ws, stream)
+        for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+            outs_host[n].copy_(t, non_blocking=True)
+        lse_host.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return ms, h2d, d2h
+
+
+def cpu_baseline_sample(name, budget_s=20.0):
+    """The fp64 oracle, as it stands, on the host cores over a bounded sample of heads."""
+    import oracle
+    inp = inputs.workload_inputs(name)
+    B, H, N, d = inp.q.shape
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    done = 0
+    t0 = time.perf_counter()
+    for b, h in heads:
+        oracle.attention_backward(inp.q[b:b + 1, h:h + 1], inp.k[b:b + 1, h:h + 1], inp.v[b:b + 1, h:h + 1],
+                                  inp.dout[b:b + 1, h:h + 1], inp.scale, causal=inp.causal,
+                                  kv_len=None if inp.kv_len is None else inp.kv_len[b:b + 1],
+                                  block_mask=inp.block_mask)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    flops = 3.5 * formula_fwd_flops(1, done, N, d, inp.causal)
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.default_threads(), "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd on {done} of {B * H} heads of {name} ({dt:.1f} s)"}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import io_aware_exact_attention_gb300 as fa
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    fa.load()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    sampler = ClockSampler(local)
+    inp, ms, pairs, _ = time_workload(args.workload, args.steps, args.warmup, torch, fa, flush,
+                                      dist if world > 1 else None, sampler)
+    B, H, N, d = inp.q.shape
+    causal = inputs.WORKLOADS[args.workload]["causal"]
+    fwd_formula = formula_fwd_flops(B, H, N, d, causal)
+    step_ms = reduce_max_over_ranks(ms["step"], dist if world > 1 else None)
+    fwd_ms = reduce_max_over_ranks(ms["fwd"], dist if world > 1 else None)
+    value = aggregate_line(3.5 * fwd_formula, world, step_ms, args.steps)
+    fwd_tflops = aggregate_line(fwd_formula, world, fwd_ms, args.steps)
+    peaks = load_peaks()
+    alg = algorithmic_flops(pairs, d)
+    kern = {"fwd": (ms["fwd"], alg["fwd"]), "bwd_main": (ms["bwd_main"], alg["bwd"])}
+    dom = max(kern, key=lambda k2: kern[k2][0])
+    dur_ms, flops = kern[dom]
+    achieved = flops / (dur_ms * 1e-3) / 1e12
+    traffic = recorded_traffic(dom, args.workload)
+    clocks = sampler.summary()
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d, "causal": causal,
+                   "key_padding": inp.kv_len is not None, "block_mask": inp.block_mask is not None,
+                   "seed": inp.seed, "l2": "flushed between timed steps (512 MiB written)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "fwd_tflops": round(fwd_tflops, 3),
+        "fwd_frac_of_peak": round(fwd_tflops / peaks["bf16_tflops"], 4),
+        "fwd_bwd_frac_of_peak": round(value / world / peaks["bf16_tflops"], 4),
+        "stage_ms": {k2: round(v2, 5) for k2, v2 in ms.items() if k2 != "wall_s"},
+        "flops_per_step": {"formula_fwd": fwd_formula, "formula_fwd_bwd": 3.5 * fwd_formula,
+                           "visited_tile_pairs": pairs, "algorithmic_fwd": alg["fwd"], "algorithmic_bwd": alg["bwd"]},
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
+                     "peak_source": f"bf16_tflops burst, {peaks['source']}"},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_e2e:
+        e2e_ms, h2d, d2h = e2e_throughput(inp, max(10, min(args.steps, 200)), torch, fa)
+        line["e2e"] = {"value": round(3.5 * fwd_formula / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)}
+    if rank == 0 and world == 1 and not args.no_extra and args.workload != EXTRA_WORKLOAD:
+        xin, xms, xpairs, _ = time_workload(EXTRA_WORKLOAD, max(3, min(args.steps, 10)), 3, torch, fa, flush)
+        xB, xH, xN, xd = xin.q.shape
+        xf = formula_fwd_flops(xB, xH, xN, xd, True)
+        xbwd_ms = xms["bwd_preprocess"] + xms["bwd_main"] + xms["bwd_postprocess"]
+        line["long_causal_16k"] = {
+            "fwd_tflops": round(xf / (xms["fwd"] * 1e-3) / 1e12, 2),
+            "bwd_tflops": round(2.5 * xf / (xbwd_ms * 1e-3) / 1e12, 2),
+            "fwd_frac_of_peak": round(xf / (xms["fwd"] * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "bwd_frac_of_peak": round(2.5 * xf / (xbwd_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "stage_ms": {k2: round(v2, 4) for k2, v2 in xms.items() if k2 != "wall_s"},
+        }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(args.workload, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle as the reference arm: one head of the workload per step on the host cores."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and rank != 0:
+        return
+    import oracle
+    inp = inputs.workload_inputs(args.workload)
+    B, H, N, d = inp.q.shape
+    heads = [(b, h) for b in range(B) for h in range(H)]
+
+    def step(i):
+        b, h = heads[i % len(heads)]
+        oracle.attention_backward(inp.q[b:b + 1, h:h + 1], inp.k[b:b + 1, h:h + 1], inp.v[b:b + 1, h:h + 1],
+                                  inp.dout[b:b + 1, h:h + 1], inp.scale, causal=inp.causal,
+                                  kv_len=None if inp.kv_len is None else inp.kv_len[b:b + 1],
+                                  block_mask=inp.block_mask)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    flops = 3.5 * formula_fwd_flops(1, 1, N, d, inp.causal) * args.steps
+    value = flops / dt / 1e12
+    sample = f"fp64 oracle fwd+bwd, one head of {args.workload} per step ({args.steps} steps, {dt:.1f} s)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d,
+                       "sample": "one head per step, cycling over all heads"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.default_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="bert_large_padded", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.workload == "tiny_fp32":
+        ap.error("tiny_fp32 is a parity case (fp32, forward only), not a bench workload")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

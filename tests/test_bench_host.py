@@ -1,0 +1,83 @@
+"""Host-side logic of bench.py, on CPU: FLOP accounting, clock parsing, the
+multi-rank (gloo, world size 2) max-over-ranks timing and the reference arm."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_flop_conventions():
+    assert bench.formula_fwd_flops(1, 32, 16384, 128, True) == pytest.approx(2.199e12, rel=1e-3)
+    assert bench.formula_fwd_flops(16, 16, 512, 64, False) == pytest.approx(17.18e9, rel=1e-3)
+
+
+def test_visited_tile_pairs():
+    assert bench.visited_tile_pairs(512, True, None, None, 1, 1) == 10
+    assert bench.visited_tile_pairs(512, False, None, None, 2, 3) == 6 * 16
+    # key padding: lengths 129 and 512 -> 2 and 4 key tiles for each of 4 query tiles
+    assert bench.visited_tile_pairs(512, False, np.array([129, 512]), None, 2, 1) == 4 * 2 + 4 * 4
+    bm = np.eye(4, dtype=np.uint8)
+    assert bench.visited_tile_pairs(512, False, None, bm, 1, 2) == 8
+    assert bench.visited_tile_pairs(300, True, None, None, 1, 1) == 6  # T = 3
+
+
+def test_clock_parsing():
+    lines = ["0, 1965, 2070, 900.1, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+             "0, 1980, 2070, 950.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+             "0, 1950, 2070, 990.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active"]
+    s = bench.parse_clock_lines(lines)
+    assert s["sm_mhz"] == 1965 and s["sm_max_mhz"] == 2070 and s["reasons"] == ["sw_power_cap"]
+    assert bench.parse_clock_lines([])["sm_mhz"] is None
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    slowest = bench.reduce_max_over_ranks(1.0 + rank, dist)
+    value = bench.aggregate_line(per_rank_flops=1e12, world=world, max_ms_step=slowest, steps=10)
+    out[rank] = (slowest, value)
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world_two():
+    port = _free_port()
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
+        res = dict(out)
+    # both ranks see the slower rank's 2 ms, and the job throughput counts both ranks' work
+    assert res[0] == res[1] == (2.0, pytest.approx(2e12 / 2e-3 / 1e12))
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "3",
+                        "--warmup", "3"], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_warmup_floor():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "1"], capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode != 0
