@@ -112,6 +112,36 @@ fa_status fa_bwd_main(const void* q, const void* k, const void* v, const float* 
 fa_status fa_bwd_postprocess(void* dq, const void* workspace, size_t workspace_bytes,
                              int B, int H, int N, int d, void* stream);
 
+/* Size of the scratch array fa_bwd_noalloc uses: 64 MiB, held by every GPU that
+ * loads this library until the process exits. */
+#define FA_BWD_NOALLOC_MAX_BYTES (64u * 1024u * 1024u)
+
+/* Backward pass for callers that cannot allocate device memory.  The pages have
+ * no counterpart to this entry point: it is a deployment convenience.
+ * Some callers are not allowed to allocate -- for example a plugin whose host
+ * application owns all device memory and gives it no allocator, or a
+ * latency-critical path where cudaMalloc's possible device synchronisation is
+ * unacceptable.  This call takes the same arguments as fa_bwd minus the
+ * workspace: its scratch (D and the float32 dQ accumulator) is a 64 MiB array
+ * inside the library, so it calls no cudaMalloc, cudaFree or allocating routine.
+ * Limits and behaviour:
+ *  - returns FA_ERR_INVALID_ARG, launching nothing, when the problem needs more
+ *    scratch than FA_BWD_NOALLOC_MAX_BYTES (that is, when
+ *    fa_bwd_workspace_size(B,H,N,d) > FA_BWD_NOALLOC_MAX_BYTES; for d = 64 about
+ *    258k query rows B*H*N, for d = 128 about 130k);
+ *  - the first call on a device looks up the array's device address (with that
+ *    device current) and caches it; make that first call before any stream
+ *    capture;
+ *  - every call on a device shares the one array and leaves its contents behind;
+ *    the call clears what must start at zero itself, but calls whose work
+ *    overlaps on the GPU (different streams, no ordering) race on the array and
+ *    give wrong gradients -- order them on one stream or with events.
+ * Other arguments, layouts and errors are those of fa_bwd. */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dout, void* dq, void* dk, void* dv,
+                         int B, int H, int N, int d, float scale, int causal,
+                         const uint8_t* block_mask, const int32_t* kv_len, int dtype, void* stream);
+
 /* Synchronises `stream`, then returns and clears the device status word:
  * FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if the synchronisation itself failed. */
 fa_status fa_get_device_status(void* stream);

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libfa_gb300.so")
 
-SOURCES = ["fa_api.cu", "fa_fwd_bf16.cu", "fa_fwd_fp32.cu", "fa_bwd_bf16.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd_bf16.cu", "fa_fwd_fp32.cu", "fa_bwd_bf16.cu", "fa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
 
