@@ -149,6 +149,10 @@ fa_status fa_get_device_status(void* stream);
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(int status);
 
+/* Name of the last CUDA runtime error that made a call on this host thread return
+ * FA_ERR_CUDA ("no error" if none).  Diagnostic only. */
+const char* fa_last_cuda_error(void);
+
 /* Library ABI version (major * 100 + minor). */
 int fa_version(void);
 

@@ -96,6 +96,8 @@ def _declare(lib):
     lib.fa_get_device_status.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_last_cuda_error.argtypes = []
+    lib.fa_last_cuda_error.restype = ctypes.c_char_p
     lib.fa_version.argtypes = []
     lib.fa_version.restype = i
     return lib

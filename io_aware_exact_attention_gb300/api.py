@@ -18,7 +18,10 @@ _DTYPES = {torch.bfloat16: _lib.FA_BF16, torch.float32: _lib.FA_FP32}
 class FaError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = int(code)
-        super().__init__(f"{where}: {_lib.status_string(code)}")
+        detail = ""
+        if self.code == _lib.FA_ERR_CUDA:
+            detail = f" ({_lib.load().fa_last_cuda_error().decode()})"
+        super().__init__(f"{where}: {_lib.status_string(code)}{detail}")
 
 
 def _check(code: int, where: str):

@@ -125,13 +125,21 @@ Workspace carve(void* ws, int B, int H, int N) {
   return Workspace{reinterpret_cast<float*>(p), reinterpret_cast<float*>(p + round256(rows * sizeof(float)))};
 }
 
-fa_status launch_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+fa_status launch_status(cudaError_t e) {
+  if (e == cudaSuccess) return FA_OK;
+  t_last_cuda_error = e;
+  return FA_ERR_CUDA;
+}
 
 }  // namespace
 
 extern "C" {
 
 int fa_version(void) { return 100; }
+
+const char* fa_last_cuda_error(void) { return cudaGetErrorString(t_last_cuda_error); }
 
 const char* fa_status_string(int status) {
   switch (status) {
