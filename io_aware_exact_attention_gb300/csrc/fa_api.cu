@@ -92,6 +92,20 @@ bool encode_bf16(CUtensorMap* map, const void* base, int BH, int N, int d) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// float32 [B*H, N, d] tensor (the dQ accumulator), boxes of 32 x 32 with 128-byte
+// swizzle; the backward kernel reduce-adds 32x32 blocks into it.
+bool encode_f32_acc(CUtensorMap* map, const void* base, int BH, int N, int d) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 fa::AttnArgs make_args(int B, int H, int N, int d, float scale, int causal, const uint8_t* block_mask,
                        const int32_t* kv_len) {
   fa::AttnArgs a;
@@ -216,7 +230,8 @@ fa_status fa_bwd_main(const void* q, const void* k, const void* v, const float* 
       !encode_bf16(&maps.dv, dv, BH, N, d))
     return FA_ERR_CUDA;
   const Workspace w = carve(workspace, B, H, N);
-  return launch_status(fa::launch_bwd_main_bf16(maps, lse, w.dsum, w.dq_acc, a, static_cast<cudaStream_t>(stream)));
+  if (!encode_f32_acc(&maps.dq_acc, w.dq_acc, BH, N, d)) return FA_ERR_CUDA;
+  return launch_status(fa::launch_bwd_main_bf16(maps, lse, w.dsum, a, static_cast<cudaStream_t>(stream)));
 }
 
 fa_status fa_bwd_postprocess(void* dq, const void* workspace, size_t workspace_bytes, int B, int H, int N, int d,

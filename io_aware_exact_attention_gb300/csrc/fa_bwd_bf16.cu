@@ -14,10 +14,14 @@
 //      over the query tiles Q_i that see it.  Five tcgen05 MMAs per tile pair:
 //        S = Q_i K_j^T and dP = dO_i V_j^T (TMEM, lanes = query rows),
 //        dV += P^T dO_i and dK += dS^T Q_i (TMEM accumulators, lanes = key rows),
-//        dQ_i = dS K_j (TMEM, added to the float32 accumulator with atomics).
-//      P and dS are written once to shared memory as bf16 in a 128-byte-swizzled
+//        dQ_i = dS K_j (TMEM), scaled and added into the float32 accumulator by
+//        TMA reduce-add from shared memory, 32x32 blocks at a time.
+//      P and then dS occupy one shared buffer as bf16 in a 128-byte-swizzled
 //      [query][key] layout; the same bytes serve as a K-major operand (dQ) and,
-//      read M-major, as the transposed operand (dV, dK).
+//      read M-major, as the transposed operand (dV, dK).  Q is double-buffered so
+//      the next tile's scores can start as soon as this tile's dK, dQ are issued.
+//      Roles: warp 0 TMA producer, warp 1 MMA issuer, warps 2..5 P and dS,
+//      warps 6..9 dQ drain and the dK, dV epilogue.
 //   3. postprocess: dQ (bf16) from the float32 accumulator.
 #include "fa_internal.h"
 #include "fa_tiles.cuh"
@@ -26,29 +30,31 @@
 namespace fa {
 namespace {
 
-constexpr int kBwdThreads = 192;
+constexpr int kBwdThreads = 320;
 constexpr float kLog2e = 1.44269504088896340736f;
 
 template <int D>
 struct BwdLayout {
-  static constexpr int kQStages = D == 64 ? 2 : 1;
+  static constexpr int kQStages = 2;
+  static constexpr int kDoStages = D == 64 ? 2 : 1;
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kSubBytes = kTile * 64 * 2;
+  static constexpr int kStageBytes = 32 * 32 * 4;  // one 32x32 fp32 dQ block
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kQ = kV + kTileBytes;
   static constexpr int kDO = kQ + kQStages * kTileBytes;
-  static constexpr int kP = kDO + kQStages * kTileBytes;
-  static constexpr int kDS = kP + kTile * kTile * 2;
-  static constexpr int kEnd = kDS + kTile * kTile * 2;
+  static constexpr int kPS = kDO + kDoStages * kTileBytes;   // P, then dS, of the current tile pair
+  static constexpr int kDQ = kPS + kTile * kTile * 2;        // 4 warps x 2 buffers of 32x32 fp32
+  static constexpr int kEnd = kDQ + 4 * 2 * kStageBytes;
   static constexpr int kSmemBytes = kEnd + 1024;
-  // TMEM columns
+  // TMEM columns.  At d = 128 the dQ tile lives in dP's columns (dP is consumed before dQ is formed).
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColDP = 128;
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
-  static constexpr bool kDqAliasesS = (256 + 3 * D) > 512;
-  static constexpr uint32_t kColDQ = kDqAliasesS ? 0u : static_cast<uint32_t>(256 + 2 * D);
+  static constexpr bool kDqAliasesDP = (256 + 3 * D) > 512;
+  static constexpr uint32_t kColDQ = kDqAliasesDP ? kColDP : static_cast<uint32_t>(256 + 2 * D);
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
@@ -56,22 +62,36 @@ struct BwdLayout {
 template <int D>
 struct BwdBarriers {
   uint64_t kv_full;
-  uint64_t qdo_full[BwdLayout<D>::kQStages];
-  uint64_t qdo_empty[BwdLayout<D>::kQStages];
+  uint64_t q_full[BwdLayout<D>::kQStages];
+  uint64_t q_empty[BwdLayout<D>::kQStages];
+  uint64_t do_full[BwdLayout<D>::kDoStages];
+  uint64_t do_empty[BwdLayout<D>::kDoStages];
   uint64_t s_full, dp_full, p_full, dv_done, ds_full, dkdq_done, dq_free, drain;
 };
 
 __device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000); }
+
+// 3-D tiled reduce-add of one box from shared memory into global memory (bulk group).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* smem_src, int c0, int c1,
+                                                  int c2) {
+  asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::
+                   "l"(reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(smem_src))
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                    const float* __restrict__ lse, const float* __restrict__ dsum, float* __restrict__ dq_acc,
-                    const AttnArgs a) {
+                    const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse,
+                    const float* __restrict__ dsum, const AttnArgs a) {
   using L = BwdLayout<D>;
   constexpr int QS = L::kQStages;
+  constexpr int DS = L::kDoStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) BwdBarriers<D> bar;
@@ -92,15 +112,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* smV = smem + L::kV;
   uint8_t* smQ = smem + L::kQ;
   uint8_t* smDO = smem + L::kDO;
-  uint8_t* smP = smem + L::kP;
-  uint8_t* smDS = smem + L::kDS;
+  uint8_t* smPS = smem + L::kPS;
+  uint8_t* smDQ = smem + L::kDQ;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar.kv_full, 1);
     for (int s = 0; s < QS; ++s) {
-      mbar_init(&bar.qdo_full[s], 1);
-      mbar_init(&bar.qdo_empty[s], 1);
+      mbar_init(&bar.q_full[s], 1);
+      mbar_init(&bar.q_empty[s], 1);
+    }
+    for (int s = 0; s < DS; ++s) {
+      mbar_init(&bar.do_full[s], 1);
+      mbar_init(&bar.do_empty[s], 1);
     }
     mbar_init(&bar.s_full, 1);
     mbar_init(&bar.dp_full, 1);
@@ -120,13 +144,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
+  const int first = next_query_tile(qt_first, kt, kv_len, a.causal, a.block_mask, T);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      const int first = next_query_tile(qt_first, kt, kv_len, a.causal, a.block_mask, T);
       if (first < T) {
         mbar_arrive_expect_tx(&bar.kv_full, 2 * L::kTileBytes);
         for (int h = 0; h < D / 64; ++h) {
@@ -135,18 +159,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       for (int qt = first; qt < T; qt = next_query_tile(qt + 1, kt, kv_len, a.causal, a.block_mask, T), ++it) {
-        const int s = it % QS;
-        if (it >= QS && !(ok = mbar_wait(&bar.qdo_empty[s], ((it / QS) - 1) & 1, wc))) break;
-        mbar_arrive_expect_tx(&bar.qdo_full[s], 2 * L::kTileBytes);
-        for (int h = 0; h < D / 64; ++h) {
-          tma_load_3d(smQ + s * L::kTileBytes + h * L::kSubBytes, &tm_q, &bar.qdo_full[s], h * 64, qt * kTile, head);
-          tma_load_3d(smDO + s * L::kTileBytes + h * L::kSubBytes, &tm_do, &bar.qdo_full[s], h * 64, qt * kTile,
+        const int sq = it % QS, sd = it % DS;
+        if (it >= QS && !(ok = mbar_wait(&bar.q_empty[sq], ((it / QS) - 1) & 1, wc))) break;
+        mbar_arrive_expect_tx(&bar.q_full[sq], L::kTileBytes);
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(smQ + sq * L::kTileBytes + h * L::kSubBytes, &tm_q, &bar.q_full[sq], h * 64, qt * kTile, head);
+        if (it >= DS && !(ok = mbar_wait(&bar.do_empty[sd], ((it / DS) - 1) & 1, wc))) break;
+        mbar_arrive_expect_tx(&bar.do_full[sd], L::kTileBytes);
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(smDO + sd * L::kTileBytes + h * L::kSubBytes, &tm_do, &bar.do_full[sd], h * 64, qt * kTile,
                       head);
-        }
       }
       if (!ok) {
+        // let the loads already issued land before the CTA can exit
         if (first < T) mbar_drain(&bar.kv_full, 0, 100000000ull);
-        for (int j = (it > QS ? it - QS : 0); j < it; ++j) mbar_drain(&bar.qdo_full[j % QS], (j / QS) & 1, 100000000ull);
+        for (int j = (it > QS ? it - QS : 0); j <= it; ++j) mbar_drain(&bar.q_full[j % QS], (j / QS) & 1, 100000000ull);
+        for (int j = (it > DS ? it - DS : 0); j < it; ++j) mbar_drain(&bar.do_full[j % DS], (j / DS) & 1, 100000000ull);
       }
     }
   } else if (warp == 1) {
@@ -155,19 +183,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);   // S, dP
       constexpr uint32_t id_t = idesc_bf16_f32(128, D, true, true);       // dV, dK (transposed A)
       constexpr uint32_t id_q = idesc_bf16_f32(128, D, false, true);      // dQ
-      const uint32_t k0 = smem_u32(smK), v0 = smem_u32(smV), p0 = smem_u32(smP), ds0 = smem_u32(smDS);
+      const uint32_t k0 = smem_u32(smK), v0 = smem_u32(smV), ps0 = smem_u32(smPS);
       bool ok = true;
       int it = 0;
-      const int first = next_query_tile(qt_first, kt, kv_len, a.causal, a.block_mask, T);
       if (first < T) ok = mbar_wait(&bar.kv_full, 0, wc);
       if (ok) {
         for (int qt = first; qt < T; qt = next_query_tile(qt + 1, kt, kv_len, a.causal, a.block_mask, T), ++it) {
-          const int s = it % QS;
-          const uint32_t q0 = smem_u32(smQ + s * L::kTileBytes), do0 = smem_u32(smDO + s * L::kTileBytes);
-          if (!(ok = mbar_wait(&bar.qdo_full[s], (it / QS) & 1, wc))) break;
-          if (L::kDqAliasesS && it >= 1 && !(ok = mbar_wait(&bar.dq_free, (it - 1) & 1, wc))) break;
+          const int sq = it % QS, sd = it % DS;
+          const uint32_t q0 = smem_u32(smQ + sq * L::kTileBytes), do0 = smem_u32(smDO + sd * L::kTileBytes);
+          // S = Q_i K_j^T (the S columns are free: P_{i-1} was read before p_full_{i-1})
+          if (!(ok = mbar_wait(&bar.q_full[sq], (it / QS) & 1, wc))) break;
           tc_fence_after();
-          // S = Q_i K_j^T and dP = dO_i V_j^T
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
@@ -175,6 +201,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         k > 0 ? 1u : 0u);
           }
           mma_commit(&bar.s_full);
+          // dP = dO_i V_j^T (when dQ shares dP's columns, the previous dQ must have been drained)
+          if (!(ok = mbar_wait(&bar.do_full[sd], (it / DS) & 1, wc))) break;
+          if (L::kDqAliasesDP && it >= 1 && !(ok = mbar_wait(&bar.dq_free, (it - 1) & 1, wc))) break;
+          tc_fence_after();
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
@@ -187,24 +217,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k)
-            mma_bf16_ss(tmem + L::kColDV, sdesc_sw128(p0 + k * 2048, L::kSubBytes, 1024),
+            mma_bf16_ss(tmem + L::kColDV, sdesc_sw128(ps0 + k * 2048, L::kSubBytes, 1024),
                         sdesc_sw128(do0 + k * 2048, L::kSubBytes, 1024), id_t, (it > 0 || k > 0) ? 1u : 0u);
           mma_commit(&bar.dv_done);
+          mma_commit(&bar.do_empty[sd]);
           // dK += dS^T Q_i ; dQ_i = dS K_j
           if (!(ok = mbar_wait(&bar.ds_full, it & 1, wc))) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k)
-            mma_bf16_ss(tmem + L::kColDK, sdesc_sw128(ds0 + k * 2048, L::kSubBytes, 1024),
+            mma_bf16_ss(tmem + L::kColDK, sdesc_sw128(ps0 + k * 2048, L::kSubBytes, 1024),
                         sdesc_sw128(q0 + k * 2048, L::kSubBytes, 1024), id_t, (it > 0 || k > 0) ? 1u : 0u);
-          if (!L::kDqAliasesS && it >= 1 && !(ok = mbar_wait(&bar.dq_free, (it - 1) & 1, wc))) break;
+          if (!L::kDqAliasesDP && it >= 1 && !(ok = mbar_wait(&bar.dq_free, (it - 1) & 1, wc))) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k)
-            mma_bf16_ss(tmem + L::kColDQ, sdesc_sw128(ds0 + (k / 4) * L::kSubBytes + (k % 4) * 32, 16, 1024),
+            mma_bf16_ss(tmem + L::kColDQ, sdesc_sw128(ps0 + (k / 4) * L::kSubBytes + (k % 4) * 32, 16, 1024),
                         sdesc_sw128(k0 + k * 2048, L::kSubBytes, 1024), id_q, k > 0 ? 1u : 0u);
           mma_commit(&bar.dkdq_done);
-          mma_commit(&bar.qdo_empty[s]);
+          mma_commit(&bar.q_empty[sq]);
         }
       }
       if (!ok) {
@@ -212,24 +243,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_drain(&bar.drain, 0, 100000000ull);
       }
     }
-  } else {
-    // ---------------------------------------------- P, dS, dQ and the epilogue
+  } else if (warp < 6) {
+    // ------------------------------------------------- P and dS (warps 2..5)
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;  // query row (for S, dP, dQ) or key row (for dK, dV) inside the tile
+    const int r = wq * 32 + lane;  // query row inside the tile
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const float sl2 = a.scale_log2;
     const int key0 = kt * kTile;
+    const uint32_t psrow = smem_u32(smPS);
     bool ok = true;
     int it = 0;
-    const int first = next_query_tile(qt_first, kt, kv_len, a.causal, a.block_mask, T);
-    for (int qt = first; qt < T; qt = next_query_tile(qt + 1, kt, kv_len, a.causal, a.block_mask, T), ++it) {
+    int qt = first;
+    // per-row statistics of the current query tile, loaded one tile ahead
+    auto load_stats = [&](int t, float& lse_v, float& d_v) {
+      const int row = t * kTile + r;
+      if (t < T && row < a.N) {
+        const size_t idx = static_cast<size_t>(head) * a.N + row;
+        lse_v = lse[idx];
+        d_v = dsum[idx];
+      } else {
+        lse_v = pos_inf();
+        d_v = 0.f;
+      }
+    };
+    float lse_r, d_r;
+    load_stats(qt, lse_r, d_r);
+    for (; qt < T; ++it) {
+      const int qt_next = next_query_tile(qt + 1, kt, kv_len, a.causal, a.block_mask, T);
+      float lse_n, d_n;
+      load_stats(qt_next, lse_n, d_n);
       const int q_row = qt * kTile + r;
-      const bool row_ok = q_row < a.N;
-      const size_t row_idx = static_cast<size_t>(head) * a.N + q_row;
-      float lse_r = row_ok ? lse[row_idx] : pos_inf();
       if (lse_r == -pos_inf()) lse_r = pos_inf();  // a row that sees no key contributes nothing
       const float lse2 = lse_r * kLog2e;
-      const float d_r = row_ok ? dsum[row_idx] : 0.f;
       const bool need_mask = (key0 + kTile > kv_len) || (a.causal && kt == qt);
       const int lim = a.causal ? min(kv_len, q_row + 1) : kv_len;  // keys [key0, lim) visible
 
@@ -253,13 +298,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       if (it >= 1) {
-        ok = mbar_wait(&bar.dv_done, (it - 1) & 1, wc);  // P_{i-1} no longer read by the dV MMA
+        ok = mbar_wait(&bar.dkdq_done, (it - 1) & 1, wc);  // dS_{i-1} no longer read by the dK, dQ MMAs
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       }
-      const uint32_t prow = smem_u32(smP);
 #pragma unroll
       for (int g = 0; g < kTile / 8; ++g)
-        st_shared_v4(prow + (g / 8) * L::kSubBytes + sw128_offset(r, g % 8), pk[4 * g], pk[4 * g + 1],
+        st_shared_v4(psrow + (g / 8) * L::kSubBytes + sw128_offset(r, g % 8), pk[4 * g], pk[4 * g + 1],
                      pk[4 * g + 2], pk[4 * g + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
@@ -268,9 +312,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = mbar_wait(&bar.dp_full, it & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      // dS_{i-1} is free: the dK/dQ MMAs that read it completed (waited at the end of the previous tile),
-      // so each 32-column chunk of dS goes to shared memory as soon as it is formed.
-      const uint32_t dsrow = smem_u32(smDS);
+      // dS replaces P in the shared buffer once the dV MMA has read P: the first two
+      // 32-column chunks are formed first, then written after that wait.
+      uint32_t w01[32];
 #pragma unroll
       for (int c0 = 0; c0 < kTile; c0 += 32) {
         uint32_t t[32];
@@ -283,44 +327,81 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const float ds1 = bf16hi(pp) * (__uint_as_float(t[i + 1]) - d_r);
           w[i / 2] = pack_bf16x2(ds0, ds1);
         }
+        if (c0 < 64) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int g = c0 / 8 + q;
-          st_shared_v4(dsrow + (g / 8) * L::kSubBytes + sw128_offset(r, g % 8), w[4 * q], w[4 * q + 1],
-                       w[4 * q + 2], w[4 * q + 3]);
+          for (int i = 0; i < 16; ++i) w01[(c0 / 2) + i] = w[i];
+          if (c0 == 32) {
+            ok = mbar_wait(&bar.dv_done, it & 1, wc);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              st_shared_v4(psrow + sw128_offset(r, g), w01[4 * g], w01[4 * g + 1], w01[4 * g + 2], w01[4 * g + 3]);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int g = c0 / 8 + q;
+            st_shared_v4(psrow + (g / 8) * L::kSubBytes + sw128_offset(r, g % 8), w[4 * q], w[4 * q + 1],
+                         w[4 * q + 2], w[4 * q + 3]);
+          }
         }
       }
+      if (!ok) break;
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bar.ds_full);
-
-      // dQ_i partial: scale * dS K_j, added into the float32 accumulator
+      qt = qt_next;
+      lse_r = lse_n;
+      d_r = d_n;
+    }
+  } else {
+    // ------------------------------- dQ drain and the dK, dV epilogue (warps 6..9)
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // query row (dQ) or key row (dK, dV) inside the tile
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    uint8_t* stage_dq = smDQ + wq * 2 * L::kStageBytes;  // this warp's two 32x32 fp32 staging blocks
+    bool ok = true;
+    int it = 0;
+    int nblk = 0;
+    for (int qt = first; qt < T; qt = next_query_tile(qt + 1, kt, kv_len, a.causal, a.block_mask, T), ++it) {
+      // dQ_i partial = dS K_j in TMEM: scale it and add it into the float32 accumulator
       ok = mbar_wait(&bar.dkdq_done, it & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      float* dq_row = dq_acc + row_idx * D;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = 0; c0 < D; c0 += 32, ++nblk) {
         uint32_t t[32];
         tmem_ld32(tmem + lane_off + L::kColDQ + c0, t);
-        if (row_ok) {
+        uint8_t* blk = stage_dq + (nblk & 1) * L::kStageBytes;
+        if (lane == 0) bulk_wait_read_le1();  // the block written two steps ago has been read
+        __syncwarp();
+        const uint32_t row = smem_u32(blk);
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            float4 v4 = make_float4(__uint_as_float(t[i]) * a.scale, __uint_as_float(t[i + 1]) * a.scale,
-                                    __uint_as_float(t[i + 2]) * a.scale, __uint_as_float(t[i + 3]) * a.scale);
-            atomicAdd(reinterpret_cast<float4*>(dq_row + c0 + i), v4);
-          }
+        for (int q = 0; q < 8; ++q)
+          st_shared_v4(row + sw128_offset(lane, q), __float_as_uint(__uint_as_float(t[4 * q]) * a.scale),
+                       __float_as_uint(__uint_as_float(t[4 * q + 1]) * a.scale),
+                       __float_as_uint(__uint_as_float(t[4 * q + 2]) * a.scale),
+                       __float_as_uint(__uint_as_float(t[4 * q + 3]) * a.scale));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&tm_dq, blk, c0, qt * kTile + wq * 32, head);
+          tma_store_commit();
         }
       }
       tc_fence_before();
       mbar_arrive(&bar.dq_free);
     }
+    if (lane == 0) tma_store_wait_all();
 
-    // epilogue: dV_j and scale * dK_j as bf16 through shared memory and TMA.
+    // epilogue: dV_j and scale * dK_j as bf16 through shared memory (the two Q
+    // stages, idle now) and TMA.  Every MMA has completed: the last dkdq_done was
+    // waited above and follows all earlier MMAs.
     const bool have = ok && it > 0;
-    // all MMAs completed: the last dkdq_done was waited above, and it follows every earlier MMA
     tc_fence_after();
-    const uint32_t stage_v = smem_u32(smQ), stage_k = smem_u32(smDO);
+    uint8_t* stv = smQ;
+    uint8_t* stk = smQ + L::kTileBytes;
+    const uint32_t stage_v = smem_u32(stv), stage_k = smem_u32(stk);
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 32) {
       uint32_t tv[32], tk[32];
@@ -346,10 +427,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     fence_proxy_async_smem();
     named_barrier(1, 128);
-    if (warp == 2 && lane == 0) {
+    if (warp == 6 && lane == 0) {
       for (int h = 0; h < D / 64; ++h) {
-        tma_store_3d(&tm_dv, smQ + h * L::kSubBytes, h * 64, kt * kTile, head);
-        tma_store_3d(&tm_dk, smDO + h * L::kSubBytes, h * 64, kt * kTile, head);
+        tma_store_3d(&tm_dv, stv + h * L::kSubBytes, h * 64, kt * kTile, head);
+        tma_store_3d(&tm_dk, stk + h * L::kSubBytes, h * 64, kt * kTile, head);
       }
       tma_store_commit();
       tma_store_wait_all();
@@ -426,7 +507,7 @@ unsigned grid_for(long long work, int per_block) {
 }
 
 template <int D>
-cudaError_t launch_bwd_main_d(const BwdMaps& m, const float* lse, const float* dsum, float* dq_acc, const AttnArgs& a,
+cudaError_t launch_bwd_main_d(const BwdMaps& m, const float* lse, const float* dsum, const AttnArgs& a,
                               cudaStream_t stream) {
   using L = BwdLayout<D>;
   static bool configured = false;
@@ -438,7 +519,7 @@ cudaError_t launch_bwd_main_d(const BwdMaps& m, const float* lse, const float* d
   }
   const long long grid = static_cast<long long>(a.n_tiles) * a.B * a.H;
   bwd_main_kernel<D><<<static_cast<unsigned>(grid), kBwdThreads, L::kSmemBytes, stream>>>(
-      m.q, m.k, m.v, m.dout, m.dk, m.dv, lse, dsum, dq_acc, a);
+      m.q, m.k, m.v, m.dout, m.dk, m.dv, m.dq_acc, lse, dsum, a);
   return cudaGetLastError();
 }
 
@@ -457,10 +538,9 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* dsum, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_main_bf16(const BwdMaps& maps, const float* lse, const float* dsum, float* dq_acc,
-                                 const AttnArgs& a, cudaStream_t stream) {
-  return a.d == 64 ? launch_bwd_main_d<64>(maps, lse, dsum, dq_acc, a, stream)
-                   : launch_bwd_main_d<128>(maps, lse, dsum, dq_acc, a, stream);
+cudaError_t launch_bwd_main_bf16(const BwdMaps& maps, const float* lse, const float* dsum, const AttnArgs& a,
+                                 cudaStream_t stream) {
+  return a.d == 64 ? launch_bwd_main_d<64>(maps, lse, dsum, a, stream) : launch_bwd_main_d<128>(maps, lse, dsum, a, stream);
 }
 
 cudaError_t launch_bwd_postprocess(const float* dq_acc, void* dq, const AttnArgs& a, cudaStream_t stream) {

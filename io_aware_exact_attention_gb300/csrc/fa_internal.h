@@ -29,6 +29,7 @@ struct FwdMaps {
 
 struct BwdMaps {
   CUtensorMap q, k, v, dout, dk, dv;
+  CUtensorMap dq_acc;  // float32 [B*H, N, d], 32 x 32 boxes, 128-byte swizzle (reduce-add target)
 };
 
 cudaError_t launch_fwd_bf16(const FwdMaps& maps, float* lse, const AttnArgs& a, cudaStream_t stream);
@@ -39,8 +40,8 @@ cudaError_t launch_fwd_fp32(const float* q, const float* k, const float* v, floa
 cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* dsum, float* dq_acc,
                                   const AttnArgs& a, cudaStream_t stream);
 
-cudaError_t launch_bwd_main_bf16(const BwdMaps& maps, const float* lse, const float* dsum, float* dq_acc,
-                                 const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_main_bf16(const BwdMaps& maps, const float* lse, const float* dsum, const AttnArgs& a,
+                                 cudaStream_t stream);
 
 cudaError_t launch_bwd_postprocess(const float* dq_acc, void* dq, const AttnArgs& a, cudaStream_t stream);
 

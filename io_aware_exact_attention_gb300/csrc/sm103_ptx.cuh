@@ -241,6 +241,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 #undef FA_W8
 
+// Fire-and-forget add of four floats to a 16-byte-aligned global address.
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
 // ------------------------------------------------------------ small numerics
 
 // 2^x on the special-function unit (PTX ex2.approx, flush-to-zero).
