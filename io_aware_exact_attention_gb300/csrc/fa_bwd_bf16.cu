@@ -283,19 +283,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       uint32_t pk[kTile / 2];
 #pragma unroll
-      for (int c0 = 0; c0 < kTile; c0 += 32) {
-        uint32_t t[32];
-        tmem_ld32(tmem + lane_off + L::kColS + c0, t);
+      for (int c0 = 0; c0 < kTile; c0 += 64) {
+        uint32_t t[64];
+        tmem_ld64(tmem + lane_off + L::kColS + c0, t);
+        // all exponentials of the chunk first (independent), then the mask and the packing
+        float f[64];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float p0 = ex2(fmaf(__uint_as_float(t[i]), sl2, -lse2));
-          float p1 = ex2(fmaf(__uint_as_float(t[i + 1]), sl2, -lse2));
-          if (need_mask) {
-            if (key0 + c0 + i >= lim) p0 = 0.f;
-            if (key0 + c0 + i + 1 >= lim) p1 = 0.f;
-          }
-          pk[(c0 + i) / 2] = pack_bf16x2(p0, p1);
+        for (int i = 0; i < 64; ++i) f[i] = ex2(fmaf(__uint_as_float(t[i]), sl2, -lse2));
+        if (need_mask) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (key0 + c0 + i >= lim) f[i] = 0.f;
         }
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) pk[(c0 + i) / 2] = pack_bf16x2(f[i], f[i + 1]);
       }
       if (it >= 1) {
         ok = mbar_wait(&bar.dkdq_done, (it - 1) & 1, wc);  // dS_{i-1} no longer read by the dK, dQ MMAs
@@ -312,39 +313,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = mbar_wait(&bar.dp_full, it & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      // dS replaces P in the shared buffer once the dV MMA has read P: the first two
-      // 32-column chunks are formed first, then written after that wait.
-      uint32_t w01[32];
+      // dS replaces P in the shared buffer once the dV MMA has read P: the first
+      // 64-column half is formed first, then written after that wait.
 #pragma unroll
-      for (int c0 = 0; c0 < kTile; c0 += 32) {
-        uint32_t t[32];
-        tmem_ld32(tmem + lane_off + L::kColDP + c0, t);
-        uint32_t w[16];
+      for (int c0 = 0; c0 < kTile; c0 += 64) {
+        uint32_t t[64];
+        tmem_ld64(tmem + lane_off + L::kColDP + c0, t);
+        float f[64];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
+        for (int i = 0; i < 64; i += 2) {
           const uint32_t pp = pk[(c0 + i) / 2];
-          const float ds0 = bf16lo(pp) * (__uint_as_float(t[i]) - d_r);
-          const float ds1 = bf16hi(pp) * (__uint_as_float(t[i + 1]) - d_r);
-          w[i / 2] = pack_bf16x2(ds0, ds1);
+          f[i] = bf16lo(pp) * (__uint_as_float(t[i]) - d_r);
+          f[i + 1] = bf16hi(pp) * (__uint_as_float(t[i + 1]) - d_r);
         }
-        if (c0 < 64) {
+        uint32_t w[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) w01[(c0 / 2) + i] = w[i];
-          if (c0 == 32) {
-            ok = mbar_wait(&bar.dv_done, it & 1, wc);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-#pragma unroll
-            for (int g = 0; g < 8; ++g)
-              st_shared_v4(psrow + sw128_offset(r, g), w01[4 * g], w01[4 * g + 1], w01[4 * g + 2], w01[4 * g + 3]);
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int g = c0 / 8 + q;
-            st_shared_v4(psrow + (g / 8) * L::kSubBytes + sw128_offset(r, g % 8), w[4 * q], w[4 * q + 1],
-                         w[4 * q + 2], w[4 * q + 3]);
-          }
+        for (int i = 0; i < 64; i += 2) w[i / 2] = pack_bf16x2(f[i], f[i + 1]);
+        if (c0 == 0) {
+          ok = mbar_wait(&bar.dv_done, it & 1, wc);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         }
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          st_shared_v4(psrow + (c0 / 64) * L::kSubBytes + sw128_offset(r, g), w[4 * g], w[4 * g + 1], w[4 * g + 2],
+                       w[4 * g + 3]);
       }
       if (!ok) break;
       fence_proxy_async_smem();
@@ -369,24 +361,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32, ++nblk) {
-        uint32_t t[32];
-        tmem_ld32(tmem + lane_off + L::kColDQ + c0, t);
-        uint8_t* blk = stage_dq + (nblk & 1) * L::kStageBytes;
-        if (lane == 0) bulk_wait_read_le1();  // the block written two steps ago has been read
-        __syncwarp();
-        const uint32_t row = smem_u32(blk);
+      for (int c64 = 0; c64 < D; c64 += 64) {
+        uint32_t t[64];
+        tmem_ld64(tmem + lane_off + L::kColDQ + c64, t);
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          st_shared_v4(row + sw128_offset(lane, q), __float_as_uint(__uint_as_float(t[4 * q]) * a.scale),
-                       __float_as_uint(__uint_as_float(t[4 * q + 1]) * a.scale),
-                       __float_as_uint(__uint_as_float(t[4 * q + 2]) * a.scale),
-                       __float_as_uint(__uint_as_float(t[4 * q + 3]) * a.scale));
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_reduce_add_3d(&tm_dq, blk, c0, qt * kTile + wq * 32, head);
-          tma_store_commit();
+        for (int h = 0; h < 2; ++h, ++nblk) {
+          uint8_t* blk = stage_dq + (nblk & 1) * L::kStageBytes;
+          if (lane == 0) bulk_wait_read_le1();  // the block written two steps ago has been read
+          __syncwarp();
+          const uint32_t row = smem_u32(blk);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            st_shared_v4(row + sw128_offset(lane, q), __float_as_uint(__uint_as_float(t[32 * h + 4 * q]) * a.scale),
+                         __float_as_uint(__uint_as_float(t[32 * h + 4 * q + 1]) * a.scale),
+                         __float_as_uint(__uint_as_float(t[32 * h + 4 * q + 2]) * a.scale),
+                         __float_as_uint(__uint_as_float(t[32 * h + 4 * q + 3]) * a.scale));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_3d(&tm_dq, blk, c64 + 32 * h, qt * kTile + wq * 32, head);
+            tma_store_commit();
+          }
         }
       }
       tc_fence_before();

@@ -241,11 +241,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_after();
         float s[kTile];
 #pragma unroll
-        for (int c0 = 0; c0 < kTile; c0 += 32) {
-          uint32_t t[32];
-          tmem_ld32(t_s + c0, t);
+        for (int c0 = 0; c0 < kTile; c0 += 64) {
+          uint32_t t[64];
+          tmem_ld64(t_s + c0, t);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[c0 + i] = __uint_as_float(t[i]);
+          for (int i = 0; i < 64; ++i) s[c0 + i] = __uint_as_float(t[i]);
         }
         // element mask: key padding tail, causal diagonal (the N tail is covered by kv_len <= N)
         const int key0 = kt * kTile;
@@ -267,17 +267,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const float m_new = (mx > m_run + kRescaleSlack) ? mx : m_run;
         const float m_use = (m_new == neg_inf()) ? 0.f : m_new;
         const float alpha = ex2(m_run - m_use);
-        uint32_t pk[kTile / 2];
-        float sum0 = 0.f, sum1 = 0.f;
+        // all exponentials first (independent, so they overlap), then sums and packing
 #pragma unroll
-        for (int c = 0; c < kTile; c += 2) {
-          const float p0 = ex2(fmaf(s[c], sl2, -m_use));
-          const float p1 = ex2(fmaf(s[c + 1], sl2, -m_use));
-          sum0 += p0;
-          sum1 += p1;
-          pk[c / 2] = pack_bf16x2(p0, p1);
+        for (int c = 0; c < kTile; ++c) s[c] = ex2(fmaf(s[c], sl2, -m_use));
+        float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+#pragma unroll
+        for (int c = 0; c < kTile; c += 4) {
+          sum0 += s[c];
+          sum1 += s[c + 1];
+          sum2 += s[c + 2];
+          sum3 += s[c + 3];
         }
-        l_run = l_run * alpha + (sum0 + sum1);
+        uint32_t pk[kTile / 2];
+#pragma unroll
+        for (int c = 0; c < kTile; c += 2) pk[c / 2] = pack_bf16x2(s[c], s[c + 1]);
+        l_run = l_run * alpha + ((sum0 + sum1) + (sum2 + sum3));
         m_run = m_new;
         // P replaces S in the tile's TMEM buffer (bf16 pairs, columns [0, 64))
         tmem_st32(t_s, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
