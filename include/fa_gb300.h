@@ -146,6 +146,13 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
  * FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if the synchronisation itself failed. */
 fa_status fa_get_device_status(void* stream);
 
+/* Failure-path self-test (no counterpart in the pages): enqueues one small
+ * kernel whose bounded wait on a barrier that nothing arrives on gives up after
+ * about one second and records FA_ERR_TIMEOUT in the device status word, exactly
+ * as a stalled attention kernel would.  Nothing faults or hangs; a following
+ * fa_get_device_status(stream) returns FA_ERR_TIMEOUT and clears the word. */
+fa_status fa_selftest_wait_timeout(void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(int status);
 

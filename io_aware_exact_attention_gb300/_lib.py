@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libfa_gb300.so")
 
-SOURCES = ["fa_api.cu", "fa_fwd_bf16.cu", "fa_fwd_fp32.cu", "fa_bwd_bf16.cu", "fa_noalloc.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd_bf16.cu", "fa_fwd_fp32.cu", "fa_bwd_bf16.cu", "fa_noalloc.cu", "fa_selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
 
@@ -92,6 +92,8 @@ def _declare(lib):
     lib.fa_bwd_main.restype = i
     lib.fa_bwd_postprocess.argtypes = [vp, vp, sz, i, i, i, i, vp]
     lib.fa_bwd_postprocess.restype = i
+    lib.fa_selftest_wait_timeout.argtypes = [vp]
+    lib.fa_selftest_wait_timeout.restype = i
     lib.fa_get_device_status.argtypes = [vp]
     lib.fa_get_device_status.restype = i
     lib.fa_status_string.argtypes = [i]

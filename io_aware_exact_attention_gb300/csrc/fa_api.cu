@@ -267,6 +267,12 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   return fa_bwd_postprocess(dq, workspace, workspace_bytes, B, H, N, d, stream);
 }
 
+fa_status fa_selftest_wait_timeout(void* stream) {
+  unsigned int* word = status_word();
+  if (word == nullptr) return FA_ERR_CUDA;
+  return launch_status(fa::launch_wait_timeout_selftest(word, static_cast<cudaStream_t>(stream)));
+}
+
 fa_status fa_get_device_status(void* stream) {
   unsigned int* word = status_word();
   if (word == nullptr) return FA_ERR_CUDA;

@@ -43,6 +43,8 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* dsum, 
 cudaError_t launch_bwd_main_bf16(const BwdMaps& maps, const float* lse, const float* dsum, const AttnArgs& a,
                                  cudaStream_t stream);
 
+cudaError_t launch_wait_timeout_selftest(unsigned int* status, cudaStream_t stream);
+
 cudaError_t launch_bwd_postprocess(const float* dq_acc, void* dq, const AttnArgs& a, cudaStream_t stream);
 
 }  // namespace fa
