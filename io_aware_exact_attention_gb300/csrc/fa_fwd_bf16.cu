@@ -169,37 +169,47 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
       const uint32_t q0 = smem_u32(smQ), k0 = smem_u32(smK), v0 = smem_u32(smV);
       bool ok = mbar_wait(&bar.q_full, 0, wc);
-      int n[2] = {0, 0};
-      int u = 0;
-      if (ok) {
-        for (int kt = next_union_tile(qt, 0, kv_len, a); kt < T; kt = next_union_tile(qt, kt + 1, kv_len, a), ++u) {
-          const int s = u % S;
-          bool f[2];
-          f[0] = tile_pair_visible(qt[0], kt, kv_len, a.causal, a.block_mask, T);
-          f[1] = has_b && tile_pair_visible(qt[1], kt, kv_len, a.causal, a.block_mask, T);
-          if (!(ok = mbar_wait(&bar.k_full[s], (u / S) & 1, wc))) break;
-          const uint32_t ks = k0 + s * L::kTileBytes;
+      int n[2] = {0, 0};  // P V products issued per query tile
+      int u = 0;          // position in the union list of key tiles
+      // S_i for key tile kt into tile i's TMEM buffer (which holds P of its last P V until that is done)
+      auto issue_scores = [&](int i, int kt_s, int stage) -> bool {
+        if (n[i] > 0 && !mbar_wait(&bar.o_done[i], (n[i] - 1) & 1, wc)) return false;
+        tc_fence_after();
+        const uint32_t qs = q0 + i * L::kTileBytes, ks = k0 + stage * L::kTileBytes;
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            if (!f[i]) continue;
-            // the score buffer still holds P of the previous tile until that P V is done
-            if (n[i] > 0 && !(ok = mbar_wait(&bar.o_done[i], (n[i] - 1) & 1, wc))) break;
-            tc_fence_after();
-            const uint32_t qs = q0 + i * L::kTileBytes;
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
+          mma_bf16_ss(tmem + L::col_s(i), sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + off, 16, 1024), idesc_s,
+                      k > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar.s_full[i]);
+        (void)kt_s;
+        return true;
+      };
+      int kt = next_union_tile(qt, 0, kv_len, a);
+      if (ok && kt < T) {
+        ok = mbar_wait(&bar.k_full[0], 0, wc);
+        for (int i = 0; ok && i < 2; ++i)
+          if (i == 0 || has_b)
+            if (tile_pair_visible(qt[i], kt, kv_len, a.causal, a.block_mask, T)) ok = issue_scores(i, kt, 0);
+      }
+      // Per key tile: P_i V for each tile i, and right after it tile i's scores for the
+      // next key tile, so each softmax warpgroup gets its next scores without waiting
+      // for the other tile.
+      while (ok && kt < T) {
+        const int s = u % S;
+        const int kt_next = next_union_tile(qt, kt + 1, kv_len, a);
+        bool f[2], fn[2];
+        f[0] = tile_pair_visible(qt[0], kt, kv_len, a.causal, a.block_mask, T);
+        f[1] = has_b && tile_pair_visible(qt[1], kt, kv_len, a.causal, a.block_mask, T);
+        fn[0] = kt_next < T && tile_pair_visible(qt[0], kt_next, kv_len, a.causal, a.block_mask, T);
+        fn[1] = kt_next < T && has_b && tile_pair_visible(qt[1], kt_next, kv_len, a.causal, a.block_mask, T);
+        if (!(ok = mbar_wait(&bar.v_full[s], (u / S) & 1, wc))) break;
+        const uint32_t vs = v0 + s * L::kTileBytes;
+        bool next_k_ready = false;
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-              const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
-              mma_bf16_ss(tmem + L::col_s(i), sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + off, 16, 1024),
-                          idesc_s, k > 0 ? 1u : 0u);
-            }
-            mma_commit(&bar.s_full[i]);
-          }
-          if (!ok) break;
-          if (!(ok = mbar_wait(&bar.v_full[s], (u / S) & 1, wc))) break;
-          const uint32_t vs = v0 + s * L::kTileBytes;
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            if (!f[i]) continue;
+        for (int i = 0; i < 2; ++i) {
+          if (f[i]) {
             if (!(ok = mbar_wait(&bar.p_full[i], n[i] & 1, wc))) break;
             tc_fence_after();
 #pragma unroll
@@ -209,9 +219,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mma_commit(&bar.o_done[i]);
             ++n[i];
           }
-          if (!ok) break;
-          mma_commit(&bar.kv_empty[s]);
+          if (fn[i]) {
+            if (!next_k_ready) {
+              if (!(ok = mbar_wait(&bar.k_full[(u + 1) % S], ((u + 1) / S) & 1, wc))) break;
+              next_k_ready = true;
+            }
+            if (!(ok = issue_scores(i, kt_next, (u + 1) % S))) break;
+          }
         }
+        if (!ok) break;
+        mma_commit(&bar.kv_empty[s]);
+        kt = kt_next;
+        ++u;
       }
       if (!ok) {
         mma_commit(&bar.drain);
