@@ -186,21 +186,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t k0 = smem_u32(smK), v0 = smem_u32(smV), ps0 = smem_u32(smPS);
       bool ok = true;
       int it = 0;
-      if (first < T) ok = mbar_wait(&bar.kv_full, 0, wc);
+      // S = Q_i K_j^T into the S columns (free once the previous P has been read out)
+      auto issue_scores = [&](int stage) {
+        const uint32_t q_s = smem_u32(smQ + stage * L::kTileBytes);
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
+          mma_bf16_ss(tmem + L::kColS, sdesc_sw128(q_s + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024), id_s,
+                      k > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar.s_full);
+      };
+      if (first < T) {
+        ok = mbar_wait(&bar.kv_full, 0, wc) && mbar_wait(&bar.q_full[0], 0, wc);
+        if (ok) issue_scores(0);
+      }
       if (ok) {
-        for (int qt = first; qt < T; qt = next_query_tile(qt + 1, kt, kv_len, a.causal, a.block_mask, T), ++it) {
+        // Per query tile: dP, dV, then the next tile's scores (so the P/dS warps can
+        // move straight on to the next tile), then dK and dQ.
+        for (int qt = first; qt < T; ++it) {
+          const int qt_next = next_query_tile(qt + 1, kt, kv_len, a.causal, a.block_mask, T);
           const int sq = it % QS, sd = it % DS;
           const uint32_t q0 = smem_u32(smQ + sq * L::kTileBytes), do0 = smem_u32(smDO + sd * L::kTileBytes);
-          // S = Q_i K_j^T (the S columns are free: P_{i-1} was read before p_full_{i-1})
-          if (!(ok = mbar_wait(&bar.q_full[sq], (it / QS) & 1, wc))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
-            mma_bf16_ss(tmem + L::kColS, sdesc_sw128(q0 + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024), id_s,
-                        k > 0 ? 1u : 0u);
-          }
-          mma_commit(&bar.s_full);
           // dP = dO_i V_j^T (when dQ shares dP's columns, the previous dQ must have been drained)
           if (!(ok = mbar_wait(&bar.do_full[sd], (it / DS) & 1, wc))) break;
           if (L::kDqAliasesDP && it >= 1 && !(ok = mbar_wait(&bar.dq_free, (it - 1) & 1, wc))) break;
@@ -221,6 +229,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         sdesc_sw128(do0 + k * 2048, L::kSubBytes, 1024), id_t, (it > 0 || k > 0) ? 1u : 0u);
           mma_commit(&bar.dv_done);
           mma_commit(&bar.do_empty[sd]);
+          // next tile's scores: the S columns were read out before p_full
+          if (qt_next < T) {
+            if (!(ok = mbar_wait(&bar.q_full[(it + 1) % QS], ((it + 1) / QS) & 1, wc))) break;
+            issue_scores((it + 1) % QS);
+          }
           // dK += dS^T Q_i ; dQ_i = dS K_j
           if (!(ok = mbar_wait(&bar.ds_full, it & 1, wc))) break;
           tc_fence_after();
@@ -236,6 +249,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         sdesc_sw128(k0 + k * 2048, L::kSubBytes, 1024), id_q, k > 0 ? 1u : 0u);
           mma_commit(&bar.dkdq_done);
           mma_commit(&bar.q_empty[sq]);
+          qt = qt_next;
         }
       }
       if (!ok) {
