@@ -303,7 +303,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // all exponentials of the chunk first (independent), then the mask and the packing
         float f[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) f[i] = ex2(fmaf(__uint_as_float(t[i]), sl2, -lse2));
+        for (int i = 0; i < 64; i += 2) {
+          ffma2(f[i], f[i + 1], __uint_as_float(t[i]), __uint_as_float(t[i + 1]), sl2, -lse2);
+          f[i] = ex2(f[i]);
+          f[i + 1] = ex2(f[i + 1]);
+        }
         if (need_mask) {
 #pragma unroll
           for (int i = 0; i < 64; ++i)
@@ -337,8 +341,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
           const uint32_t pp = pk[(c0 + i) / 2];
-          f[i] = bf16lo(pp) * (__uint_as_float(t[i]) - d_r);
-          f[i + 1] = bf16hi(pp) * (__uint_as_float(t[i + 1]) - d_r);
+          fsubmul2(f[i], f[i + 1], __uint_as_float(t[i]), __uint_as_float(t[i + 1]), d_r, bf16lo(pp), bf16hi(pp));
         }
         uint32_t w[32];
 #pragma unroll

@@ -274,28 +274,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int c = 0; c < kTile; ++c)
             if (key0 + c >= lim) s[c] = neg_inf();
         }
-        float mx0 = neg_inf(), mx1 = neg_inf(), mx2 = neg_inf(), mx3 = neg_inf();
+        float mx0 = neg_inf(), mx1 = neg_inf();
 #pragma unroll
         for (int c = 0; c < kTile; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
+          mx0 = fmax3(mx0, s[c], s[c + 1]);
+          mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
         }
-        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const float mx = fmaxf(mx0, mx1) * sl2;
         const float m_new = (mx > m_run + kRescaleSlack) ? mx : m_run;
         const float m_use = (m_new == neg_inf()) ? 0.f : m_new;
         const float alpha = ex2(m_run - m_use);
-        // all exponentials first (independent, so they overlap), then sums and packing
+        // all exponentials first (independent, so they overlap), then sums and packing;
+        // scale-and-subtract and the sums run two lanes per instruction
 #pragma unroll
-        for (int c = 0; c < kTile; ++c) s[c] = ex2(fmaf(s[c], sl2, -m_use));
+        for (int c = 0; c < kTile; c += 2) {
+          ffma2(s[c], s[c + 1], s[c], s[c + 1], sl2, -m_use);
+          s[c] = ex2(s[c]);
+          s[c + 1] = ex2(s[c + 1]);
+        }
         float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
 #pragma unroll
         for (int c = 0; c < kTile; c += 4) {
-          sum0 += s[c];
-          sum1 += s[c + 1];
-          sum2 += s[c + 2];
-          sum3 += s[c + 3];
+          fadd2(sum0, sum1, s[c], s[c + 1]);
+          fadd2(sum2, sum3, s[c + 2], s[c + 3]);
         }
         uint32_t pk[kTile / 2];
 #pragma unroll
