@@ -171,9 +171,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       bool ok = mbar_wait(&bar.q_full, 0, wc);
       int n[2] = {0, 0};  // P V products issued per query tile
       int u = 0;          // position in the union list of key tiles
-      // S_i for key tile kt into tile i's TMEM buffer (which holds P of its last P V until that is done)
+      // S_i for key tile kt into tile i's TMEM buffer.  That buffer still holds P_i of the
+      // last P V, which this thread issued earlier: MMAs from one thread execute in issue
+      // order, so the new scores overwrite P only after that P V has read it.
       auto issue_scores = [&](int i, int kt_s, int stage) -> bool {
-        if (n[i] > 0 && !mbar_wait(&bar.o_done[i], (n[i] - 1) & 1, wc)) return false;
         tc_fence_after();
         const uint32_t qs = q0 + i * L::kTileBytes, ks = k0 + stage * L::kTileBytes;
 #pragma unroll
