@@ -30,33 +30,39 @@
 namespace fa {
 namespace {
 
-constexpr int kFwdThreads = 320;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleSlack = 8.0f;  // P values stay below 2^8 before a rescale is forced
 
-template <int D>
+// NQ query tiles per CTA.  NQ = 2 (d = 128): one CTA per SM, the two tiles'
+// softmax phases overlap each other's MMAs.  NQ = 1 (d = 64): a lighter CTA with
+// 256 TMEM columns and ~81 KB of shared memory, so two CTAs share an SM and one
+// CTA's set-up, loads and epilogue overlap the other's main loop.
+template <int D, int NQ>
 struct FwdLayout {
-  static constexpr int kStages = D == 64 ? 4 : 2;
+  static constexpr int kThreads = 64 + 128 * NQ;  // producer warp, MMA warp, one softmax warpgroup per tile
+  static constexpr int kCtasPerSm = NQ == 1 ? 2 : 1;
+  static constexpr int kStages = NQ == 1 ? 2 : (D == 64 ? 4 : 2);
   static constexpr int kTileBytes = kTile * D * 2;  // one 128-row tile of Q, K or V (bf16)
   static constexpr int kSubBytes = kTile * 64 * 2;  // one 64-column swizzle sub-tile
-  static constexpr int kQ = 0;                      // two query tiles
-  static constexpr int kK = kQ + 2 * kTileBytes;
+  static constexpr int kQ = 0;                      // NQ query tiles
+  static constexpr int kK = kQ + NQ * kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
   static constexpr int kEnd = kV + kStages * kTileBytes;
   static constexpr int kSmemBytes = kEnd + 1024;  // slack for aligning the base to 1024
-  static constexpr uint32_t kTmemCols = 512;
-  // TMEM columns: score/P buffer of tile i at 128*i, output accumulator of tile i at 256 + D*i
+  static constexpr uint32_t kTmemCols = NQ == 1 ? 256 : 512;
+  // TMEM columns: score/P buffer of tile i at 128*i, output accumulator of tile i after all score buffers
   __device__ static constexpr uint32_t col_s(int i) { return 128u * static_cast<uint32_t>(i); }
-  __device__ static constexpr uint32_t col_o(int i) { return 256u + static_cast<uint32_t>(D * i); }
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  __device__ static constexpr uint32_t col_o(int i) { return 128u * NQ + static_cast<uint32_t>(D * i); }
+  static_assert(128 * NQ + D * NQ <= static_cast<int>(kTmemCols), "TMEM budget");
+  static_assert(kSmemBytes <= (NQ == 1 ? 112 * 1024 : 227 * 1024), "shared memory budget");
 };
 
-template <int D>
+template <int D, int NQ>
 struct FwdBarriers {
   uint64_t q_full;
-  uint64_t k_full[FwdLayout<D>::kStages];
-  uint64_t v_full[FwdLayout<D>::kStages];
-  uint64_t kv_empty[FwdLayout<D>::kStages];
+  uint64_t k_full[FwdLayout<D, NQ>::kStages];
+  uint64_t v_full[FwdLayout<D, NQ>::kStages];
+  uint64_t kv_empty[FwdLayout<D, NQ>::kStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
@@ -76,27 +82,27 @@ __device__ __forceinline__ int next_union_tile(const int (&qt)[2], int kt, int k
   return kt;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kFwdThreads, 1)
+template <int D, int NQ>
+__global__ void __launch_bounds__(FwdLayout<D, NQ>::kThreads, FwdLayout<D, NQ>::kCtasPerSm)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     float* __restrict__ lse_out, const AttnArgs a) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, NQ>;
   constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) FwdBarriers<D> bar;
+  __shared__ __align__(8) FwdBarriers<D, NQ> bar;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int T = a.n_tiles;
-  const int n_pairs = (T + 1) / 2;
-  const int head = blockIdx.x / n_pairs;  // b * H + h
-  const int pr = static_cast<int>(blockIdx.x % n_pairs);
-  const int pair = a.causal ? (n_pairs - 1 - pr) : pr;  // causal: heaviest pairs first
-  const int qt[2] = {2 * pair, 2 * pair + 1};
+  const int n_groups = (T + NQ - 1) / NQ;
+  const int head = blockIdx.x / n_groups;  // b * H + h
+  const int gr = static_cast<int>(blockIdx.x % n_groups);
+  const int group = a.causal ? (n_groups - 1 - gr) : gr;  // causal: heaviest groups first
+  const int qt[2] = {NQ * group, NQ == 2 ? 2 * group + 1 : T};  // qt[1] >= T: no second tile
   const bool has_b = qt[1] < T;
   const int b = head / a.H;
   const int kv_len = clamp_kv_len(a.kv_len, b, a.N);
@@ -376,22 +382,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D>
+template <int D, int NQ>
 cudaError_t launch_fwd_d(const FwdMaps& maps, float* lse, const AttnArgs& a, cudaStream_t stream) {
-  using L = FwdLayout<D>;
-  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  using L = FwdLayout<D, NQ>;
+  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        L::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long grid = static_cast<long long>((a.n_tiles + 1) / 2) * a.B * a.H;
-  fwd_bf16_kernel<D><<<static_cast<unsigned>(grid), kFwdThreads, L::kSmemBytes, stream>>>(maps.q, maps.k, maps.v,
-                                                                                         maps.o, lse, a);
+  const long long grid = static_cast<long long>((a.n_tiles + NQ - 1) / NQ) * a.B * a.H;
+  fwd_bf16_kernel<D, NQ><<<static_cast<unsigned>(grid), L::kThreads, L::kSmemBytes, stream>>>(maps.q, maps.k, maps.v,
+                                                                                             maps.o, lse, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const FwdMaps& maps, float* lse, const AttnArgs& a, cudaStream_t stream) {
-  return a.d == 64 ? launch_fwd_d<64>(maps, lse, a, stream) : launch_fwd_d<128>(maps, lse, a, stream);
+  return a.d == 64 ? launch_fwd_d<64, 1>(maps, lse, a, stream) : launch_fwd_d<128, 2>(maps, lse, a, stream);
 }
 
 }  // namespace fa
