@@ -56,6 +56,10 @@ struct BwdLayout {
   static constexpr bool kDqAliasesDP = (256 + 3 * D) > 512;
   static constexpr uint32_t kColDQ = kDqAliasesDP ? kColDP : static_cast<uint32_t>(256 + 2 * D);
   static constexpr uint32_t kTmemCols = 512;
+  // d = 64: the P/dS work (a full 128-key row per thread regardless of d) is split by
+  // key halves over both compute warpgroups, each also draining its half of dQ.
+  static constexpr bool kSplitCols = (D == 64);
+  static constexpr uint32_t kComputeArrivals = kSplitCols ? 256u : 128u;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -128,11 +132,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(&bar.s_full, 1);
     mbar_init(&bar.dp_full, 1);
-    mbar_init(&bar.p_full, 128);
+    mbar_init(&bar.p_full, L::kComputeArrivals);
     mbar_init(&bar.dv_done, 1);
-    mbar_init(&bar.ds_full, 128);
+    mbar_init(&bar.ds_full, L::kComputeArrivals);
     mbar_init(&bar.dkdq_done, 1);
-    mbar_init(&bar.dq_free, 128);
+    mbar_init(&bar.dq_free, L::kComputeArrivals);
     mbar_init(&bar.drain, 1);
     fence_mbar_init();
   }
@@ -256,6 +260,177 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_commit(&bar.drain);
         mbar_drain(&bar.drain, 0, 100000000ull);
       }
+    }
+  } else if (L::kSplitCols) {
+    // ------------- d = 64: P, dS and the dQ drain split by key halves (warps 2..9)
+    const int hc = (warp - 2) >> 2;  // keys [64 hc, 64 hc + 64) of P and dS; dQ, dK, dV columns [32 hc, 32 hc + 32)
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // query row (P, dS, dQ) or key row (dK, dV) inside the tile
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const float sl2 = a.scale_log2;
+    const int key0 = kt * kTile + 64 * hc;
+    const uint32_t psrow = smem_u32(smPS) + hc * L::kSubBytes;
+    uint8_t* blk = smDQ + (hc * 4 + wq) * L::kStageBytes;  // this warp's 32x32 fp32 dQ staging block
+    bool ok = true;
+    int it = 0;
+    int qt = first, qt_prev = first;
+    auto load_stats = [&](int t, float& lse_v, float& d_v) {
+      const int row = t * kTile + r;
+      if (t < T && row < a.N) {
+        const size_t idx = static_cast<size_t>(head) * a.N + row;
+        lse_v = lse[idx];
+        d_v = dsum[idx];
+      } else {
+        lse_v = pos_inf();
+        d_v = 0.f;
+      }
+    };
+    // dQ of query tile qt_d (this warp's 32 rows x 32 columns): TMEM -> swizzled
+    // shared block -> TMA reduce-add into the float32 accumulator
+    auto drain_dq = [&](int qt_d) {
+      uint32_t t[32];
+      tmem_ld32(tmem + lane_off + L::kColDQ + 32 * hc, t);
+      if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // last block read
+      __syncwarp();
+      const uint32_t row = smem_u32(blk);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st_shared_v4(row + sw128_offset(lane, q), __float_as_uint(__uint_as_float(t[4 * q]) * a.scale),
+                     __float_as_uint(__uint_as_float(t[4 * q + 1]) * a.scale),
+                     __float_as_uint(__uint_as_float(t[4 * q + 2]) * a.scale),
+                     __float_as_uint(__uint_as_float(t[4 * q + 3]) * a.scale));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_3d(&tm_dq, blk, 32 * hc, qt_d * kTile + wq * 32, head);
+        tma_store_commit();
+      }
+    };
+    float lse_r, d_r;
+    load_stats(qt, lse_r, d_r);
+    for (; qt < T; ++it) {
+      const int qt_next = next_query_tile(qt + 1, kt, kv_len, a.causal, a.block_mask, T);
+      float lse_n, d_n;
+      load_stats(qt_next, lse_n, d_n);
+      const int q_row = qt * kTile + r;
+      if (lse_r == -pos_inf()) lse_r = pos_inf();  // a row that sees no key contributes nothing
+      const float lse2 = lse_r * kLog2e;
+      const bool need_mask = (kt * kTile + kTile > kv_len) || (a.causal && kt == qt);
+      const int lim = a.causal ? min(kv_len, q_row + 1) : kv_len;  // keys [kt*128, lim) visible
+
+      ok = mbar_wait(&bar.s_full, it & 1, wc);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t pk[32];
+      {
+        uint32_t t[64];
+        tmem_ld64(tmem + lane_off + L::kColS + 64 * hc, t);
+        float f[64];
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          ffma2(f[i], f[i + 1], __uint_as_float(t[i]), __uint_as_float(t[i + 1]), sl2, -lse2);
+          f[i] = ex2(f[i]);
+          f[i + 1] = ex2(f[i + 1]);
+        }
+        if (need_mask) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (key0 + i >= lim) f[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+      }
+      if (it >= 1) {
+        // the previous dK, dQ MMAs are done: dS_{i-1} is no longer read, and dQ_{i-1} is ready
+        ok = mbar_wait(&bar.dkdq_done, (it - 1) & 1, wc);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        drain_dq(qt_prev);
+        tc_fence_before();
+        mbar_arrive(&bar.dq_free);
+      }
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        st_shared_v4(psrow + sw128_offset(r, g), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar.p_full);
+
+      ok = mbar_wait(&bar.dp_full, it & 1, wc);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t w[32];
+      {
+        uint32_t t[64];
+        tmem_ld64(tmem + lane_off + L::kColDP + 64 * hc, t);
+        float f[64];
+#pragma unroll
+        for (int i = 0; i < 64; i += 2)
+          fsubmul2(f[i], f[i + 1], __uint_as_float(t[i]), __uint_as_float(t[i + 1]), d_r, bf16lo(pk[i / 2]),
+                   bf16hi(pk[i / 2]));
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+      }
+      // dS replaces P in the shared buffer once the dV MMA has read P
+      ok = mbar_wait(&bar.dv_done, it & 1, wc);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        st_shared_v4(psrow + sw128_offset(r, g), w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar.ds_full);
+      qt_prev = qt;
+      qt = qt_next;
+      lse_r = lse_n;
+      d_r = d_n;
+    }
+    // the last tile's dQ
+    if (ok && it > 0) {
+      ok = mbar_wait(&bar.dkdq_done, (it - 1) & 1, wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        drain_dq(qt_prev);
+      }
+    }
+    if (lane == 0) tma_store_wait_all();
+
+    // epilogue: this warpgroup's 32 columns of dV_j and scale * dK_j as bf16 into the
+    // (idle) Q stages, then one TMA store of each tile
+    const bool have = ok && it > 0;
+    tc_fence_after();
+    uint8_t* stv = smQ;
+    uint8_t* stk = smQ + L::kTileBytes;
+    {
+      uint32_t tv[32], tk[32];
+      if (have) {
+        tmem_ld32(tmem + lane_off + L::kColDV + 32 * hc, tv);
+        tmem_ld32(tmem + lane_off + L::kColDK + 32 * hc, tk);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) tv[i] = tk[i] = 0u;
+      }
+      uint32_t wv[16], wk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        wv[i] = pack_bf16x2(__uint_as_float(tv[2 * i]), __uint_as_float(tv[2 * i + 1]));
+        wk[i] = pack_bf16x2(__uint_as_float(tk[2 * i]) * a.scale, __uint_as_float(tk[2 * i + 1]) * a.scale);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t off = sw128_offset(r, 4 * hc + q);
+        st_shared_v4(smem_u32(stv) + off, wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
+        st_shared_v4(smem_u32(stk) + off, wk[4 * q], wk[4 * q + 1], wk[4 * q + 2], wk[4 * q + 3]);
+      }
+    }
+    fence_proxy_async_smem();
+    named_barrier(1, 256);
+    if (warp == 2 && lane == 0) {
+      tma_store_3d(&tm_dv, stv, 0, kt * kTile, head);
+      tma_store_3d(&tm_dk, stk, 0, kt * kTile, head);
+      tma_store_commit();
+      tma_store_wait_all();
     }
   } else if (warp < 6) {
     // ------------------------------------------------- P and dS (warps 2..5)
