@@ -22,6 +22,9 @@
 //      the next tile's scores can start as soon as this tile's dK, dQ are issued.
 //      Roles: warp 0 TMA producer, warp 1 MMA issuer, warps 2..5 P and dS,
 //      warps 6..9 dQ drain and the dK, dV epilogue.
+//      At d = 64 the main step is a persistent kernel instead: one CTA per SM walks
+//      key tiles with two K/V buffers, and both compute warpgroups share P, dS and
+//      the dQ drain by key halves (bwd_persistent_kernel).
 //   3. postprocess: dQ (bf16) from the float32 accumulator.
 #include "fa_internal.h"
 #include "fa_tiles.cuh"
@@ -56,10 +59,7 @@ struct BwdLayout {
   static constexpr bool kDqAliasesDP = (256 + 3 * D) > 512;
   static constexpr uint32_t kColDQ = kDqAliasesDP ? kColDP : static_cast<uint32_t>(256 + 2 * D);
   static constexpr uint32_t kTmemCols = 512;
-  // d = 64: the P/dS work (a full 128-key row per thread regardless of d) is split by
-  // key halves over both compute warpgroups, each also draining its half of dQ.
-  static constexpr bool kSplitCols = (D == 64);
-  static constexpr uint32_t kComputeArrivals = kSplitCols ? 256u : 128u;
+  static constexpr uint32_t kComputeArrivals = 128u;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -261,177 +261,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_drain(&bar.drain, 0, 100000000ull);
       }
     }
-  } else if (L::kSplitCols) {
-    // ------------- d = 64: P, dS and the dQ drain split by key halves (warps 2..9)
-    const int hc = (warp - 2) >> 2;  // keys [64 hc, 64 hc + 64) of P and dS; dQ, dK, dV columns [32 hc, 32 hc + 32)
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;  // query row (P, dS, dQ) or key row (dK, dV) inside the tile
-    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const float sl2 = a.scale_log2;
-    const int key0 = kt * kTile + 64 * hc;
-    const uint32_t psrow = smem_u32(smPS) + hc * L::kSubBytes;
-    uint8_t* blk = smDQ + (hc * 4 + wq) * L::kStageBytes;  // this warp's 32x32 fp32 dQ staging block
-    bool ok = true;
-    int it = 0;
-    int qt = first, qt_prev = first;
-    auto load_stats = [&](int t, float& lse_v, float& d_v) {
-      const int row = t * kTile + r;
-      if (t < T && row < a.N) {
-        const size_t idx = static_cast<size_t>(head) * a.N + row;
-        lse_v = lse[idx];
-        d_v = dsum[idx];
-      } else {
-        lse_v = pos_inf();
-        d_v = 0.f;
-      }
-    };
-    // dQ of query tile qt_d (this warp's 32 rows x 32 columns): TMEM -> swizzled
-    // shared block -> TMA reduce-add into the float32 accumulator
-    auto drain_dq = [&](int qt_d) {
-      uint32_t t[32];
-      tmem_ld32(tmem + lane_off + L::kColDQ + 32 * hc, t);
-      if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // last block read
-      __syncwarp();
-      const uint32_t row = smem_u32(blk);
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        st_shared_v4(row + sw128_offset(lane, q), __float_as_uint(__uint_as_float(t[4 * q]) * a.scale),
-                     __float_as_uint(__uint_as_float(t[4 * q + 1]) * a.scale),
-                     __float_as_uint(__uint_as_float(t[4 * q + 2]) * a.scale),
-                     __float_as_uint(__uint_as_float(t[4 * q + 3]) * a.scale));
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_reduce_add_3d(&tm_dq, blk, 32 * hc, qt_d * kTile + wq * 32, head);
-        tma_store_commit();
-      }
-    };
-    float lse_r, d_r;
-    load_stats(qt, lse_r, d_r);
-    for (; qt < T; ++it) {
-      const int qt_next = next_query_tile(qt + 1, kt, kv_len, a.causal, a.block_mask, T);
-      float lse_n, d_n;
-      load_stats(qt_next, lse_n, d_n);
-      const int q_row = qt * kTile + r;
-      if (lse_r == -pos_inf()) lse_r = pos_inf();  // a row that sees no key contributes nothing
-      const float lse2 = lse_r * kLog2e;
-      const bool need_mask = (kt * kTile + kTile > kv_len) || (a.causal && kt == qt);
-      const int lim = a.causal ? min(kv_len, q_row + 1) : kv_len;  // keys [kt*128, lim) visible
-
-      ok = mbar_wait(&bar.s_full, it & 1, wc);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t pk[32];
-      {
-        uint32_t t[64];
-        tmem_ld64(tmem + lane_off + L::kColS + 64 * hc, t);
-        float f[64];
-#pragma unroll
-        for (int i = 0; i < 64; i += 2) {
-          ffma2(f[i], f[i + 1], __uint_as_float(t[i]), __uint_as_float(t[i + 1]), sl2, -lse2);
-          f[i] = ex2(f[i]);
-          f[i + 1] = ex2(f[i + 1]);
-        }
-        if (need_mask) {
-#pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (key0 + i >= lim) f[i] = 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-      }
-      if (it >= 1) {
-        // the previous dK, dQ MMAs are done: dS_{i-1} is no longer read, and dQ_{i-1} is ready
-        ok = mbar_wait(&bar.dkdq_done, (it - 1) & 1, wc);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-        drain_dq(qt_prev);
-        tc_fence_before();
-        mbar_arrive(&bar.dq_free);
-      }
-#pragma unroll
-      for (int g = 0; g < 8; ++g)
-        st_shared_v4(psrow + sw128_offset(r, g), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bar.p_full);
-
-      ok = mbar_wait(&bar.dp_full, it & 1, wc);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t w[32];
-      {
-        uint32_t t[64];
-        tmem_ld64(tmem + lane_off + L::kColDP + 64 * hc, t);
-        float f[64];
-#pragma unroll
-        for (int i = 0; i < 64; i += 2)
-          fsubmul2(f[i], f[i + 1], __uint_as_float(t[i]), __uint_as_float(t[i + 1]), d_r, bf16lo(pk[i / 2]),
-                   bf16hi(pk[i / 2]));
-#pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-      }
-      // dS replaces P in the shared buffer once the dV MMA has read P
-      ok = mbar_wait(&bar.dv_done, it & 1, wc);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-#pragma unroll
-      for (int g = 0; g < 8; ++g)
-        st_shared_v4(psrow + sw128_offset(r, g), w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bar.ds_full);
-      qt_prev = qt;
-      qt = qt_next;
-      lse_r = lse_n;
-      d_r = d_n;
-    }
-    // the last tile's dQ
-    if (ok && it > 0) {
-      ok = mbar_wait(&bar.dkdq_done, (it - 1) & 1, wc);
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok) {
-        tc_fence_after();
-        drain_dq(qt_prev);
-      }
-    }
-    if (lane == 0) tma_store_wait_all();
-
-    // epilogue: this warpgroup's 32 columns of dV_j and scale * dK_j as bf16 into the
-    // (idle) Q stages, then one TMA store of each tile
-    const bool have = ok && it > 0;
-    tc_fence_after();
-    uint8_t* stv = smQ;
-    uint8_t* stk = smQ + L::kTileBytes;
-    {
-      uint32_t tv[32], tk[32];
-      if (have) {
-        tmem_ld32(tmem + lane_off + L::kColDV + 32 * hc, tv);
-        tmem_ld32(tmem + lane_off + L::kColDK + 32 * hc, tk);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) tv[i] = tk[i] = 0u;
-      }
-      uint32_t wv[16], wk[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        wv[i] = pack_bf16x2(__uint_as_float(tv[2 * i]), __uint_as_float(tv[2 * i + 1]));
-        wk[i] = pack_bf16x2(__uint_as_float(tk[2 * i]) * a.scale, __uint_as_float(tk[2 * i + 1]) * a.scale);
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t off = sw128_offset(r, 4 * hc + q);
-        st_shared_v4(smem_u32(stv) + off, wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
-        st_shared_v4(smem_u32(stk) + off, wk[4 * q], wk[4 * q + 1], wk[4 * q + 2], wk[4 * q + 3]);
-      }
-    }
-    fence_proxy_async_smem();
-    named_barrier(1, 256);
-    if (warp == 2 && lane == 0) {
-      tma_store_3d(&tm_dv, stv, 0, kt * kTile, head);
-      tma_store_3d(&tm_dk, stk, 0, kt * kTile, head);
-      tma_store_commit();
-      tma_store_wait_all();
-    }
   } else if (warp < 6) {
     // ------------------------------------------------- P and dS (warps 2..5)
     const int wq = warp & 3;
@@ -632,6 +461,463 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// Persistent backward for d = 64: one CTA per SM walks key tiles c, c + G, c + 2G, ...
+// (G = grid size), with two K/V buffers so the next key tile loads while this one is
+// processed, and dV/dK staged in buffers of their own so the Q ring keeps streaming.
+// The P/dS work (a full 128-key row per thread regardless of d) is split by key halves
+// over both compute warpgroups, each also draining its half of dQ.
+template <int D>
+struct PBwdLayout {
+  static_assert(D == 64, "the persistent backward is the d = 64 kernel");
+  static constexpr int kQStages = 2;
+  static constexpr int kDoStages = 2;
+  static constexpr int kKvBuffers = 2;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kSubBytes = kTile * 64 * 2;
+  static constexpr int kStageBytes = 32 * 32 * 4;  // one 32x32 fp32 dQ block
+  static constexpr int kKV = 0;                                   // [K, V] per buffer
+  static constexpr int kQ = kKV + kKvBuffers * 2 * kTileBytes;
+  static constexpr int kDO = kQ + kQStages * kTileBytes;
+  static constexpr int kPS = kDO + kDoStages * kTileBytes;   // P, then dS, of the current tile pair
+  static constexpr int kDQ = kPS + kTile * kTile * 2;        // 8 fp32 32x32 dQ staging blocks
+  static constexpr int kST = kDQ + 8 * kStageBytes;          // dV, dK staging
+  static constexpr int kEnd = kST + 2 * kTileBytes;
+  static constexpr int kSmemBytes = kEnd + 1024;
+  // TMEM columns: S, dP, dV, dK, dQ side by side (128 + 128 + 3 * 64 <= 512).
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColDP = 128;
+  static constexpr uint32_t kColDV = 256;
+  static constexpr uint32_t kColDK = 256 + D;
+  static constexpr uint32_t kColDQ = 256 + 2 * D;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kComputeArrivals = 256u;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+template <int D>
+struct PBwdBarriers {
+  uint64_t kv_full[PBwdLayout<D>::kKvBuffers];
+  uint64_t kv_empty[PBwdLayout<D>::kKvBuffers];
+  uint64_t q_full[PBwdLayout<D>::kQStages];
+  uint64_t q_empty[PBwdLayout<D>::kQStages];
+  uint64_t do_full[PBwdLayout<D>::kDoStages];
+  uint64_t do_empty[PBwdLayout<D>::kDoStages];
+  uint64_t s_full, dp_full, p_full, dv_done, ds_full, dkdq_done, dq_free, acc_free, drain;
+};
+
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// One unit of persistent backward work: a 128-row key tile of one (batch, head).
+struct BwdItem {
+  int head, kt, kv_len, first;  // first query tile that sees the key tile (T if none)
+};
+
+// Items are taken key-tile-major, so every CTA gets an even mix of causal work
+// (early key tiles have the most query tiles).
+__device__ __forceinline__ BwdItem bwd_item(int item, const AttnArgs& a) {
+  BwdItem w;
+  const int BH = a.B * a.H;
+  w.head = item % BH;
+  w.kt = item / BH;
+  w.kv_len = clamp_kv_len(a.kv_len, w.head / a.H, a.N);
+  w.first = next_query_tile(a.causal ? w.kt : 0, w.kt, w.kv_len, a.causal, a.block_mask, a.n_tiles);
+  return w;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                    const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse,
+                    const float* __restrict__ dsum, const AttnArgs a) {
+  using L = PBwdLayout<D>;
+  constexpr int QS = L::kQStages;
+  constexpr int DS = L::kDoStages;
+  constexpr int KB = L::kKvBuffers;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) PBwdBarriers<D> bar;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int T = a.n_tiles;
+  const int n_items = T * a.B * a.H;
+  const WaitCtx wc{&abort_flag, a.status};
+
+  uint8_t* smKV = smem + L::kKV;
+  uint8_t* smQ = smem + L::kQ;
+  uint8_t* smDO = smem + L::kDO;
+  uint8_t* smPS = smem + L::kPS;
+  uint8_t* smDQ = smem + L::kDQ;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < KB; ++s) {
+      mbar_init(&bar.kv_full[s], 1);
+      mbar_init(&bar.kv_empty[s], 1);
+    }
+    for (int s = 0; s < QS; ++s) {
+      mbar_init(&bar.q_full[s], 1);
+      mbar_init(&bar.q_empty[s], 1);
+    }
+    for (int s = 0; s < DS; ++s) {
+      mbar_init(&bar.do_full[s], 1);
+      mbar_init(&bar.do_empty[s], 1);
+    }
+    mbar_init(&bar.s_full, 1);
+    mbar_init(&bar.dp_full, 1);
+    mbar_init(&bar.p_full, L::kComputeArrivals);
+    mbar_init(&bar.dv_done, 1);
+    mbar_init(&bar.ds_full, L::kComputeArrivals);
+    mbar_init(&bar.dkdq_done, 1);
+    mbar_init(&bar.dq_free, L::kComputeArrivals);
+    mbar_init(&bar.acc_free, L::kComputeArrivals);
+    mbar_init(&bar.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_s, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int git = 0;  // query-tile iterations over all items of this CTA
+      int kvu = 0;  // items with work (K/V buffer uses)
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const BwdItem w = bwd_item(item, a);
+        if (w.first >= T) continue;  // no query sees this key tile: nothing to load
+        const int kb = kvu % KB;
+        if (kvu >= KB && !(ok = mbar_wait(&bar.kv_empty[kb], ((kvu / KB) - 1) & 1, wc))) break;
+        uint8_t* kvs = smKV + kb * 2 * L::kTileBytes;
+        mbar_arrive_expect_tx(&bar.kv_full[kb], 2 * L::kTileBytes);
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_3d(kvs + h * L::kSubBytes, &tm_k, &bar.kv_full[kb], h * 64, w.kt * kTile, w.head);
+          tma_load_3d(kvs + L::kTileBytes + h * L::kSubBytes, &tm_v, &bar.kv_full[kb], h * 64, w.kt * kTile, w.head);
+        }
+        ++kvu;
+        for (int qt = w.first; qt < T; qt = next_query_tile(qt + 1, w.kt, w.kv_len, a.causal, a.block_mask, T), ++git) {
+          const int sq = git % QS, sd = git % DS;
+          if (git >= QS && !(ok = mbar_wait(&bar.q_empty[sq], ((git / QS) - 1) & 1, wc))) break;
+          mbar_arrive_expect_tx(&bar.q_full[sq], L::kTileBytes);
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(smQ + sq * L::kTileBytes + h * L::kSubBytes, &tm_q, &bar.q_full[sq], h * 64, qt * kTile,
+                        w.head);
+          if (git >= DS && !(ok = mbar_wait(&bar.do_empty[sd], ((git / DS) - 1) & 1, wc))) break;
+          mbar_arrive_expect_tx(&bar.do_full[sd], L::kTileBytes);
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(smDO + sd * L::kTileBytes + h * L::kSubBytes, &tm_do, &bar.do_full[sd], h * 64, qt * kTile,
+                        w.head);
+        }
+      }
+      if (!ok) {
+        // let the loads already issued land before the CTA can exit
+        for (int j = (kvu > KB ? kvu - KB : 0); j < kvu; ++j)
+          mbar_drain(&bar.kv_full[j % KB], (j / KB) & 1, 100000000ull);
+        for (int j = (git > QS ? git - QS : 0); j <= git; ++j)
+          mbar_drain(&bar.q_full[j % QS], (j / QS) & 1, 100000000ull);
+        for (int j = (git > DS ? git - DS : 0); j < git; ++j)
+          mbar_drain(&bar.do_full[j % DS], (j / DS) & 1, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);   // S, dP
+      constexpr uint32_t id_t = idesc_bf16_f32(128, D, true, true);       // dV, dK (transposed A)
+      constexpr uint32_t id_q = idesc_bf16_f32(128, D, false, true);      // dQ
+      const uint32_t ps0 = smem_u32(smPS);
+      bool ok = true;
+      int git = 0, kvu = 0;
+      int accu = 0;  // items whose dK, dV accumulators were used
+      // S = Q K_j^T into the S columns (free once the previous P has been read out)
+      auto issue_scores = [&](int stage, uint32_t k0) {
+        const uint32_t q_s = smem_u32(smQ + stage * L::kTileBytes);
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
+          mma_bf16_ss(tmem + L::kColS, sdesc_sw128(q_s + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024), id_s,
+                      k > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar.s_full);
+      };
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const BwdItem w = bwd_item(item, a);
+        if (w.first >= T) continue;
+        const int kb = kvu % KB;
+        const uint32_t k0 = smem_u32(smKV + kb * 2 * L::kTileBytes), v0 = k0 + L::kTileBytes;
+        if (!(ok = mbar_wait(&bar.kv_full[kb], (kvu / KB) & 1, wc))) break;
+        if (!(ok = mbar_wait(&bar.q_full[git % QS], (git / QS) & 1, wc))) break;
+        issue_scores(git % QS, k0);
+        // Per query tile: dP, dV, then the next tile's scores (so the P/dS warps can
+        // move straight on), then dK and dQ.
+        int itl = 0;
+        for (int qt = w.first; qt < T; ++itl, ++git) {
+          const int qt_next = next_query_tile(qt + 1, w.kt, w.kv_len, a.causal, a.block_mask, T);
+          const int sq = git % QS, sd = git % DS;
+          const uint32_t q0 = smem_u32(smQ + sq * L::kTileBytes), do0 = smem_u32(smDO + sd * L::kTileBytes);
+          // dP = dO_i V_j^T (when dQ shares dP's columns, the previous dQ must have been drained)
+          if (!(ok = mbar_wait(&bar.do_full[sd], (git / DS) & 1, wc))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
+            mma_bf16_ss(tmem + L::kColDP, sdesc_sw128(do0 + off, 16, 1024), sdesc_sw128(v0 + off, 16, 1024), id_s,
+                        k > 0 ? 1u : 0u);
+          }
+          mma_commit(&bar.dp_full);
+          // dV += P^T dO_i; the first of an item overwrites the accumulators, which the
+          // previous item's epilogue must have read out
+          if (!(ok = mbar_wait(&bar.p_full, git & 1, wc))) break;
+          if (itl == 0 && accu > 0 && !(ok = mbar_wait(&bar.acc_free, (accu - 1) & 1, wc))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k)
+            mma_bf16_ss(tmem + L::kColDV, sdesc_sw128(ps0 + k * 2048, L::kSubBytes, 1024),
+                        sdesc_sw128(do0 + k * 2048, L::kSubBytes, 1024), id_t, (itl > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bar.dv_done);
+          mma_commit(&bar.do_empty[sd]);
+          // next tile's scores: the S columns were read out before p_full
+          if (qt_next < T) {
+            if (!(ok = mbar_wait(&bar.q_full[(git + 1) % QS], ((git + 1) / QS) & 1, wc))) break;
+            issue_scores((git + 1) % QS, k0);
+          }
+          // dK += dS^T Q_i ; dQ_i = dS K_j
+          if (!(ok = mbar_wait(&bar.ds_full, git & 1, wc))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k)
+            mma_bf16_ss(tmem + L::kColDK, sdesc_sw128(ps0 + k * 2048, L::kSubBytes, 1024),
+                        sdesc_sw128(q0 + k * 2048, L::kSubBytes, 1024), id_t, (itl > 0 || k > 0) ? 1u : 0u);
+          if (git >= 1 && !(ok = mbar_wait(&bar.dq_free, (git - 1) & 1, wc))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kTile / 16; ++k)
+            mma_bf16_ss(tmem + L::kColDQ, sdesc_sw128(ps0 + (k / 4) * L::kSubBytes + (k % 4) * 32, 16, 1024),
+                        sdesc_sw128(k0 + k * 2048, L::kSubBytes, 1024), id_q, k > 0 ? 1u : 0u);
+          mma_commit(&bar.dkdq_done);
+          mma_commit(&bar.q_empty[sq]);
+          qt = qt_next;
+        }
+        if (!ok) break;
+        mma_commit(&bar.kv_empty[kb]);  // K_j, V_j are free once this item's MMAs finish
+        ++kvu;
+        ++accu;
+      }
+      if (!ok) {
+        mma_commit(&bar.drain);
+        mbar_drain(&bar.drain, 0, 100000000ull);
+      }
+    }
+  } else {
+    // ------- d = 64: P, dS, the dQ drain and the dK, dV epilogue, split by halves (warps 2..9)
+    const int hc = (warp - 2) >> 2;  // keys [64 hc, 64 hc + 64) of P and dS; dQ, dK, dV columns [32 hc, 32 hc + 32)
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // query row (P, dS, dQ) or key row (dK, dV) inside the tile
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const float sl2 = a.scale_log2;
+    const uint32_t psrow = smem_u32(smPS) + hc * L::kSubBytes;
+    uint8_t* blk = smDQ + (hc * 4 + wq) * L::kStageBytes;  // this warp's 32x32 fp32 dQ staging block
+    uint8_t* stv = smem + L::kST;     // dV, dK staging
+    uint8_t* stk = stv + L::kTileBytes;
+    bool ok = true;
+    int git = 0;
+    bool pending = false;  // dQ of iteration git-1 not yet drained
+    int pend_qt = 0, pend_head = 0;
+    // dQ of query tile qt_d of head h_d (this warp's 32 rows x 32 columns): TMEM ->
+    // swizzled shared block -> TMA reduce-add into the float32 accumulator
+    auto drain_dq = [&](int qt_d, int h_d) {
+      uint32_t t[32];
+      tmem_ld32(tmem + lane_off + L::kColDQ + 32 * hc, t);
+      if (lane == 0) bulk_wait_read_all();  // the block's last reduce has read it
+      __syncwarp();
+      const uint32_t row = smem_u32(blk);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st_shared_v4(row + sw128_offset(lane, q), __float_as_uint(__uint_as_float(t[4 * q]) * a.scale),
+                     __float_as_uint(__uint_as_float(t[4 * q + 1]) * a.scale),
+                     __float_as_uint(__uint_as_float(t[4 * q + 2]) * a.scale),
+                     __float_as_uint(__uint_as_float(t[4 * q + 3]) * a.scale));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_3d(&tm_dq, blk, 32 * hc, qt_d * kTile + wq * 32, h_d);
+        tma_store_commit();
+      }
+    };
+    // Every warp walks every item and reaches both epilogue barriers even after a wait
+    // has given up (ok == false), so the named barriers always stay matched; an aborted
+    // CTA only skips the work.
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      const BwdItem w = bwd_item(item, a);
+      const bool work = w.first < T;
+      auto load_stats = [&](int t, float& lse_v, float& d_v) {
+        const int row = t * kTile + r;
+        if (t < T && row < a.N) {
+          const size_t idx = static_cast<size_t>(w.head) * a.N + row;
+          lse_v = lse[idx];
+          d_v = dsum[idx];
+        } else {
+          lse_v = pos_inf();
+          d_v = 0.f;
+        }
+      };
+      const int key0 = w.kt * kTile + 64 * hc;
+      float lse_r, d_r;
+      load_stats(w.first, lse_r, d_r);
+      for (int qt = w.first; ok && qt < T; ++git) {
+        const int qt_next = next_query_tile(qt + 1, w.kt, w.kv_len, a.causal, a.block_mask, T);
+        float lse_n, d_n;
+        load_stats(qt_next, lse_n, d_n);
+        const int q_row = qt * kTile + r;
+        if (lse_r == -pos_inf()) lse_r = pos_inf();  // a row that sees no key contributes nothing
+        const float lse2 = lse_r * kLog2e;
+        const bool need_mask = (w.kt * kTile + kTile > w.kv_len) || (a.causal && w.kt == qt);
+        const int lim = a.causal ? min(w.kv_len, q_row + 1) : w.kv_len;  // keys [kt*128, lim) visible
+
+        ok = mbar_wait(&bar.s_full, git & 1, wc);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t pk[32];
+        {
+          uint32_t t[64];
+          tmem_ld64(tmem + lane_off + L::kColS + 64 * hc, t);
+          float f[64];
+#pragma unroll
+          for (int i = 0; i < 64; i += 2) {
+            ffma2(f[i], f[i + 1], __uint_as_float(t[i]), __uint_as_float(t[i + 1]), sl2, -lse2);
+            f[i] = ex2(f[i]);
+            f[i + 1] = ex2(f[i + 1]);
+          }
+          if (need_mask) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+              if (key0 + i >= lim) f[i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+        }
+        if (git >= 1) {
+          // the previous dK, dQ MMAs are done: dS_{i-1} is no longer read, and dQ_{i-1} is ready
+          ok = mbar_wait(&bar.dkdq_done, (git - 1) & 1, wc);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          if (pending) {
+            tc_fence_after();
+            drain_dq(pend_qt, pend_head);
+            tc_fence_before();
+            mbar_arrive(&bar.dq_free);
+            pending = false;
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          st_shared_v4(psrow + sw128_offset(r, g), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bar.p_full);
+
+        ok = mbar_wait(&bar.dp_full, git & 1, wc);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t wds[32];
+        {
+          uint32_t t[64];
+          tmem_ld64(tmem + lane_off + L::kColDP + 64 * hc, t);
+          float f[64];
+#pragma unroll
+          for (int i = 0; i < 64; i += 2)
+            fsubmul2(f[i], f[i + 1], __uint_as_float(t[i]), __uint_as_float(t[i + 1]), d_r, bf16lo(pk[i / 2]),
+                     bf16hi(pk[i / 2]));
+#pragma unroll
+          for (int i = 0; i < 32; ++i) wds[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+        }
+        // dS replaces P in the shared buffer once the dV MMA has read P
+        ok = mbar_wait(&bar.dv_done, git & 1, wc);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          st_shared_v4(psrow + sw128_offset(r, g), wds[4 * g], wds[4 * g + 1], wds[4 * g + 2], wds[4 * g + 3]);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bar.ds_full);
+        pending = true;
+        pend_qt = qt;
+        pend_head = w.head;
+        qt = qt_next;
+        lse_r = lse_n;
+        d_r = d_n;
+      }
+      // end of the item: its last dK, dQ MMAs (and so all its MMAs) complete with dkdq_done
+      if (ok && work) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar.dkdq_done, (git - 1) & 1, wc));
+      }
+      if (ok && work) {
+        tc_fence_after();
+        if (pending) {
+          drain_dq(pend_qt, pend_head);
+          tc_fence_before();
+          mbar_arrive(&bar.dq_free);
+          pending = false;
+        }
+      }
+      // epilogue: this warpgroup's 32 columns of dV_j and scale * dK_j as bf16 into the
+      // staging tiles, then one TMA store of each; key tiles no query sees get zeros
+      if (warp == 2 && lane == 0) bulk_wait_read_all();  // the previous item's stores have read the staging
+      named_barrier(1, 256);
+      {
+        uint32_t tv[32], tk[32];
+        if (ok && work) {
+          tc_fence_after();
+          tmem_ld32(tmem + lane_off + L::kColDV + 32 * hc, tv);
+          tmem_ld32(tmem + lane_off + L::kColDK + 32 * hc, tk);
+          tc_fence_before();
+          mbar_arrive(&bar.acc_free);  // the accumulators may now be overwritten by the next item
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) tv[i] = tk[i] = 0u;
+        }
+        uint32_t wv[16], wk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          wv[i] = pack_bf16x2(__uint_as_float(tv[2 * i]), __uint_as_float(tv[2 * i + 1]));
+          wk[i] = pack_bf16x2(__uint_as_float(tk[2 * i]) * a.scale, __uint_as_float(tk[2 * i + 1]) * a.scale);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t off = sw128_offset(r, 4 * hc + q);
+          st_shared_v4(smem_u32(stv) + off, wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
+          st_shared_v4(smem_u32(stk) + off, wk[4 * q], wk[4 * q + 1], wk[4 * q + 2], wk[4 * q + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      named_barrier(1, 256);
+      if (warp == 2 && lane == 0) {
+        tma_store_3d(&tm_dv, stv, 0, w.kt * kTile, w.head);
+        tma_store_3d(&tm_dk, stk, 0, w.kt * kTile, w.head);
+        tma_store_commit();
+      }
+    }
+    if (lane == 0) tma_store_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
 // D_i = sum_c dO_ic O_ic (float32) for every row, and dq_acc = 0.
 // Eight bf16 per lane; D / 8 lanes share a row.
 template <int D>
@@ -696,17 +982,25 @@ unsigned grid_for(long long work, int per_block) {
 template <int D>
 cudaError_t launch_bwd_main_d(const BwdMaps& m, const float* lse, const float* dsum, const AttnArgs& a,
                               cudaStream_t stream) {
-  using L = BwdLayout<D>;
-  static bool configured = false;
-  if (!configured) {
+  const long long n_items = static_cast<long long>(a.n_tiles) * a.B * a.H;
+  if constexpr (D == 64) {
+    // persistent: one CTA per SM walks the key tiles
+    using L = PBwdLayout<D>;
+    cudaError_t e = cudaFuncSetAttribute(bwd_persistent_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const long long grid = n_items < sm_count() ? n_items : sm_count();
+    bwd_persistent_kernel<D><<<static_cast<unsigned>(grid), kBwdThreads, L::kSmemBytes, stream>>>(
+        m.q, m.k, m.v, m.dout, m.dk, m.dv, m.dq_acc, lse, dsum, a);
+  } else {
+    // one CTA per key tile
+    using L = BwdLayout<D>;
     cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured = true;
+    bwd_main_kernel<D><<<static_cast<unsigned>(n_items), kBwdThreads, L::kSmemBytes, stream>>>(
+        m.q, m.k, m.v, m.dout, m.dk, m.dv, m.dq_acc, lse, dsum, a);
   }
-  const long long grid = static_cast<long long>(a.n_tiles) * a.B * a.H;
-  bwd_main_kernel<D><<<static_cast<unsigned>(grid), kBwdThreads, L::kSmemBytes, stream>>>(
-      m.q, m.k, m.v, m.dout, m.dk, m.dv, m.dq_acc, lse, dsum, a);
   return cudaGetLastError();
 }
 
