@@ -4,9 +4,12 @@
 
 One step = one pass of the whole attention path over one batch of the workload:
 fa_fwd (one kernel) then fa_bwd's three stages (preprocess, main, postprocess),
-inputs resident in HBM.  Timed with CUDA events on the launching stream, L2
-flushed (512 MiB written) between timed steps, max over ranks.  Prints one JSON
-line (rank 0).
+inputs resident in HBM.  Each timed step calls the API (--graphs instead captures
+each stage's call once as a CUDA graph after the warm-up and replays the graphs).
+Timed with CUDA events on the launching stream between the
+stages, L2 flushed between timed steps (512 MiB written, then 256 MiB read so that
+the flush's own dirty lines are written back before the next step), max over ranks.  Prints
+one JSON line (rank 0).
 
 FLOP convention: forward 4*B*H*N^2*d (halved when causal), backward 2.5x forward;
 `value` is forward+backward TFLOP/s.  The roofline object reports the dominant
@@ -38,7 +41,25 @@ from io_aware_exact_attention_gb300 import inputs  # noqa: E402
 
 METRIC = "attention TFLOP/s fwd & fwd+bwd bf16 on 1 GB300; % of dense BF16 tensor peak"
 UNIT = "TFLOP/s"
-FLUSH_BYTES = 512 << 20
+FLUSH_BYTES = 512 << 20       # written between timed steps (L2 is 129 MB)
+FLUSH_READ_BYTES = 256 << 20  # then read, so L2 holds clean lines only when a step starts
+
+
+class L2Flush:
+    """Evicts the workload from L2 between timed steps: writes FLUSH_BYTES, then reads
+    FLUSH_READ_BYTES of another buffer.  The read pass makes L2 write back the dirty
+    lines of the write pass, so the next step starts on a cold, clean L2 instead of
+    paying for the flush's write-back in its first kernel."""
+
+    def __init__(self, torch):
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.r = torch.ones(FLUSH_READ_BYTES // 4, dtype=torch.float32, device="cuda")
+        self.acc = torch.empty((), dtype=torch.float32, device="cuda")
+        self.torch = torch
+
+    def __call__(self):
+        self.w.zero_()
+        self.torch.sum(self.r, dim=0, out=self.acc)
 TILE = 128
 EXTRA_WORKLOAD = "long_causal_16k"
 
@@ -193,8 +214,11 @@ def device_inputs(inp, torch):
     return t
 
 
-def time_workload(name, steps, warmup, torch, fa, flush, dist=None, sampler=None, override=None):
-    """Run `steps` timed fwd+bwd steps on one workload; per-stage CUDA-event times."""
+def time_workload(name, steps, warmup, torch, fa, flush, dist=None, sampler=None, override=None, graphs=False):
+    """Run `steps` timed fwd+bwd steps on one workload; per-stage CUDA-event times.
+
+    With `graphs`, each stage's API call is captured once as a CUDA graph after the
+    warm-up and the timed steps replay the graphs (same kernels, same arguments)."""
     spec = inputs.WORKLOADS[name]
     inp = inputs.workload_inputs(name, **(override or {}))
     B, H, N, d = inp.q.shape
@@ -207,25 +231,44 @@ def time_workload(name, steps, warmup, torch, fa, flush, dist=None, sampler=None
     stream = torch.cuda.current_stream()
     scale, causal = inp.scale, spec["causal"]
 
+    stages = [
+        lambda s: fa.fa_fwd(q, k, v, o, lse, scale, causal, bm, kl, s),
+        lambda s: fa.fa_bwd_preprocess(o, do, ws, s),
+        lambda s: fa.fa_bwd_main(q, k, v, lse, do, dk, dv, ws, scale, causal, bm, kl, s),
+        lambda s: fa.fa_bwd_postprocess(dq, ws, s),
+    ]
+    launch = [lambda fn=fn: fn(stream) for fn in stages]
+
     def step(ev=None):
+        for j, run in enumerate(launch):
+            if ev is not None:
+                ev[j].record(stream)
+            run()
         if ev is not None:
-            ev[0].record(stream)
-        fa.fa_fwd(q, k, v, o, lse, scale, causal, bm, kl, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        fa.fa_bwd_preprocess(o, do, ws, stream)
-        if ev is not None:
-            ev[2].record(stream)
-        fa.fa_bwd_main(q, k, v, lse, do, dk, dv, ws, scale, causal, bm, kl, stream)
-        if ev is not None:
-            ev[3].record(stream)
-        fa.fa_bwd_postprocess(dq, ws, stream)
-        if ev is not None:
-            ev[4].record(stream)
+            ev[len(launch)].record(stream)
 
     for _ in range(warmup):
-        flush.zero_()
+        flush()
         step()
+    launch_mode = "api calls"
+    if graphs:
+        torch.cuda.synchronize()
+        try:
+            captured = []
+            for fn in stages:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    fn(torch.cuda.current_stream())
+                captured.append(g)
+            torch.cuda.synchronize()
+            launch = [g.replay for g in captured]
+            launch_mode = "CUDA graph per stage, replayed"
+        except Exception as exc:  # keep measuring through the API if capture is refused
+            torch.cuda.synchronize()
+            launch_mode = f"api calls (graph capture failed: {type(exc).__name__})"
+        for _ in range(2):
+            flush()
+            step()
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
     if dist is not None and dist.is_initialized():
         dist.barrier()
@@ -234,7 +277,7 @@ def time_workload(name, steps, warmup, torch, fa, flush, dist=None, sampler=None
     with ctx:
         t0 = time.perf_counter()
         for i in range(steps):
-            flush.zero_()
+            flush()
             step(events[i])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
@@ -250,6 +293,7 @@ def time_workload(name, steps, warmup, torch, fa, flush, dist=None, sampler=None
     ms = {k2: v2 / steps for k2, v2 in stage.items()}
     ms["step"] = sum(ms.values())
     ms["wall_s"] = wall
+    ms["launch"] = launch_mode
     pairs = visited_tile_pairs(N, causal, inp.kv_len, inp.block_mask, B, H)
     return inp, ms, pairs, (q, k, v, do, bm, kl)
 
@@ -342,10 +386,10 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     fa.load()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(torch)
     sampler = ClockSampler(local)
     inp, ms, pairs, _ = time_workload(args.workload, args.steps, args.warmup, torch, fa, flush,
-                                      dist if world > 1 else None, sampler)
+                                      dist if world > 1 else None, sampler, graphs=args.graphs)
     B, H, N, d = inp.q.shape
     causal = inputs.WORKLOADS[args.workload]["causal"]
     fwd_formula = formula_fwd_flops(B, H, N, d, causal)
@@ -368,12 +412,14 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d, "causal": causal,
                    "key_padding": inp.kv_len is not None, "block_mask": inp.block_mask is not None,
-                   "seed": inp.seed, "l2": "flushed between timed steps (512 MiB written)",
+                   "seed": inp.seed, "l2": "flushed between timed steps (512 MiB written, 256 MiB read)",
+                   "launch": ms["launch"],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "fwd_tflops": round(fwd_tflops, 3),
         "fwd_frac_of_peak": round(fwd_tflops / peaks["bf16_tflops"], 4),
         "fwd_bwd_frac_of_peak": round(value / world / peaks["bf16_tflops"], 4),
-        "stage_ms": {k2: round(v2, 5) for k2, v2 in ms.items() if k2 != "wall_s"},
+        "stage_ms": {k2: round(v2, 5) for k2, v2 in ms.items() if k2 not in ("wall_s", "launch")},
+        "wall_ms_per_step": round(ms["wall_s"] / args.steps * 1e3, 5),
         "flops_per_step": {"formula_fwd": fwd_formula, "formula_fwd_bwd": 3.5 * fwd_formula,
                            "visited_tile_pairs": pairs, "algorithmic_fwd": alg["fwd"], "algorithmic_bwd": alg["bwd"]},
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
@@ -387,7 +433,8 @@ def run_ours(args):
         line["e2e"] = {"value": round(3.5 * fwd_formula / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)}
     if rank == 0 and world == 1 and not args.no_extra and args.workload != EXTRA_WORKLOAD:
-        xin, xms, xpairs, _ = time_workload(EXTRA_WORKLOAD, max(3, min(args.steps, 10)), 3, torch, fa, flush)
+        xin, xms, xpairs, _ = time_workload(EXTRA_WORKLOAD, max(3, min(args.steps, 10)), 3, torch, fa, flush,
+                                            graphs=args.graphs)
         xB, xH, xN, xd = xin.q.shape
         xf = formula_fwd_flops(xB, xH, xN, xd, True)
         xbwd_ms = xms["bwd_preprocess"] + xms["bwd_main"] + xms["bwd_postprocess"]
@@ -396,7 +443,7 @@ def run_ours(args):
             "bwd_tflops": round(2.5 * xf / (xbwd_ms * 1e-3) / 1e12, 2),
             "fwd_frac_of_peak": round(xf / (xms["fwd"] * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
             "bwd_frac_of_peak": round(2.5 * xf / (xbwd_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-            "stage_ms": {k2: round(v2, 4) for k2, v2 in xms.items() if k2 != "wall_s"},
+            "stage_ms": {k2: round(v2, 4) for k2, v2 in xms.items() if k2 not in ("wall_s", "launch")},
         }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(args.workload, args.cpu_budget)
@@ -452,6 +499,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="bert_large_padded", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--graphs", action="store_true", help="replay one CUDA graph per stage instead of calling the API")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")

@@ -10,6 +10,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "../../include/fa_gb300.h"
 #include "fa_internal.h"
@@ -92,6 +93,20 @@ bool encode_bf16(CUtensorMap* map, const void* base, int BH, int N, int d) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [B*H, N, d] bf16 tensor, boxes of 32 columns x 32 rows with 64-byte swizzle (the
+// block one warp of the d = 64 backward writes of dK or dV).
+bool encode_bf16_block32(CUtensorMap* map, const void* base, int BH, int N, int d) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // float32 [B*H, N, d] tensor (the dQ accumulator), boxes of 32 x 32 with 128-byte
 // swizzle; the backward kernel reduce-adds 32x32 blocks into it.
 bool encode_f32_acc(CUtensorMap* map, const void* base, int BH, int N, int d) {
@@ -148,6 +163,34 @@ fa_status launch_status(cudaError_t e) {
 }
 
 }  // namespace
+
+namespace fa {
+cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
+  struct Entry {
+    const void* kernel;
+    int device, bytes;
+  };
+  static std::vector<Entry> done;
+  static std::mutex mu;
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : done)
+    if (e.kernel == kernel && e.device == dev && e.bytes >= bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.push_back({kernel, dev, bytes});
+  return e;
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n = 152;
+  }
+  return n;
+}
+}  // namespace fa
 
 extern "C" {
 
@@ -231,6 +274,8 @@ fa_status fa_bwd_main(const void* q, const void* k, const void* v, const float* 
     return FA_ERR_CUDA;
   const Workspace w = carve(workspace, B, H, N);
   if (!encode_f32_acc(&maps.dq_acc, w.dq_acc, BH, N, d)) return FA_ERR_CUDA;
+  if (d == 64 && (!encode_bf16_block32(&maps.dk32, dk, BH, N, d) || !encode_bf16_block32(&maps.dv32, dv, BH, N, d)))
+    return FA_ERR_CUDA;
   return launch_status(fa::launch_bwd_main_bf16(maps, lse, w.dsum, a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -463,9 +463,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 // Persistent backward for d = 64: one CTA per SM walks key tiles c, c + G, c + 2G, ...
 // (G = grid size), with two K/V buffers so the next key tile loads while this one is
-// processed, and dV/dK staged in buffers of their own so the Q ring keeps streaming.
-// The P/dS work (a full 128-key row per thread regardless of d) is split by key halves
-// over both compute warpgroups, each also draining its half of dQ.
+// processed, and two P/dS buffers so the next P is written while dK, dQ still read
+// this dS.  The P/dS work (a full 128-key row per thread regardless of d) is split by
+// key halves over both compute warpgroups; each warp drains its 32 x 32 block of dQ
+// and writes its 32 x 32 blocks of dV, dK through one private staging block.
 template <int D>
 struct PBwdLayout {
   static_assert(D == 64, "the persistent backward is the d = 64 kernel");
@@ -478,10 +479,10 @@ struct PBwdLayout {
   static constexpr int kKV = 0;                                   // [K, V] per buffer
   static constexpr int kQ = kKV + kKvBuffers * 2 * kTileBytes;
   static constexpr int kDO = kQ + kQStages * kTileBytes;
-  static constexpr int kPS = kDO + kDoStages * kTileBytes;   // P, then dS, of the current tile pair
-  static constexpr int kDQ = kPS + kTile * kTile * 2;        // 8 fp32 32x32 dQ staging blocks
-  static constexpr int kST = kDQ + 8 * kStageBytes;          // dV, dK staging
-  static constexpr int kEnd = kST + 2 * kTileBytes;
+  static constexpr int kPSBytes = kTile * kTile * 2;
+  static constexpr int kPS = kDO + kDoStages * kTileBytes;   // 2 buffers: P, then dS, of tile pair i in buffer i % 2
+  static constexpr int kDQ = kPS + 2 * kPSBytes;             // 8 staging blocks (one per compute warp)
+  static constexpr int kEnd = kDQ + 8 * kStageBytes;
   static constexpr int kSmemBytes = kEnd + 1024;
   // TMEM columns: S, dP, dV, dK, dQ side by side (128 + 128 + 3 * 64 <= 512).
   static constexpr uint32_t kColS = 0;
@@ -502,10 +503,10 @@ struct PBwdBarriers {
   uint64_t q_empty[PBwdLayout<D>::kQStages];
   uint64_t do_full[PBwdLayout<D>::kDoStages];
   uint64_t do_empty[PBwdLayout<D>::kDoStages];
-  uint64_t s_full, dp_full, p_full, dv_done, ds_full, dkdq_done, dq_free, acc_free, drain;
+  uint64_t dkdq_done[2];  // tile pair i completes dkdq_done[i % 2]
+  uint64_t s_full, dp_full, p_full, dv_done, ds_full, dq_free, acc_free, drain;
 };
 
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // One unit of persistent backward work: a 128-row key tile of one (batch, head).
 struct BwdItem {
@@ -513,16 +514,38 @@ struct BwdItem {
 };
 
 // Items are taken key-tile-major, so every CTA gets an even mix of causal work
-// (early key tiles have the most query tiles).
-__device__ __forceinline__ BwdItem bwd_item(int item, const AttnArgs& a) {
+// (early key tiles have the most query tiles).  `kv_len_raw` is the item's entry of
+// the key-padding lengths (item_kv_len), loaded ahead so no role waits on it.
+__device__ __forceinline__ BwdItem bwd_item(int item, int kv_len_raw, const AttnArgs& a) {
   BwdItem w;
   const int BH = a.B * a.H;
   w.head = item % BH;
   w.kt = item / BH;
-  w.kv_len = clamp_kv_len(a.kv_len, w.head / a.H, a.N);
+  w.kv_len = kv_len_raw < 0 ? 0 : (kv_len_raw > a.N ? a.N : kv_len_raw);
   w.first = next_query_tile(a.causal ? w.kt : 0, w.kt, w.kv_len, a.causal, a.block_mask, a.n_tiles);
   return w;
 }
+
+// Key-padding length of item `item`'s batch (N without padding or past the last item).
+__device__ __forceinline__ int item_kv_len(int item, int n_items, const AttnArgs& a) {
+  if (a.kv_len == nullptr || item >= n_items) return a.N;
+  return a.kv_len[(item % (a.B * a.H)) / a.H];
+}
+
+// kv_len of a CTA's items two items ahead: next() returns the current item's value and
+// issues the load for the item two steps on, which has a whole item to arrive.
+struct KvLenAhead {
+  int n0, n1, step, n_items;
+  __device__ __forceinline__ KvLenAhead(int first, int g, int n, const AttnArgs& a)
+      : n0(item_kv_len(first, n, a)), n1(item_kv_len(first + g, n, a)), step(g), n_items(n) {}
+  __device__ __forceinline__ int next(int item, const AttnArgs& a) {
+    const int cur = n0;
+    n0 = n1;
+    n1 = item_kv_len(item + 2 * step, n_items, a);
+    return cur;
+  }
+  __device__ __forceinline__ int peek() const { return n0; }  // the next item's, after next()
+};
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -572,7 +595,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bar.p_full, L::kComputeArrivals);
     mbar_init(&bar.dv_done, 1);
     mbar_init(&bar.ds_full, L::kComputeArrivals);
-    mbar_init(&bar.dkdq_done, 1);
+    mbar_init(&bar.dkdq_done[0], 1);
+    mbar_init(&bar.dkdq_done[1], 1);
     mbar_init(&bar.dq_free, L::kComputeArrivals);
     mbar_init(&bar.acc_free, L::kComputeArrivals);
     mbar_init(&bar.drain, 1);
@@ -593,8 +617,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int git = 0;  // query-tile iterations over all items of this CTA
       int kvu = 0;  // items with work (K/V buffer uses)
       bool ok = true;
+      KvLenAhead kvl(blockIdx.x, gridDim.x, n_items, a);
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-        const BwdItem w = bwd_item(item, a);
+        const BwdItem w = bwd_item(item, kvl.next(item, a), a);
         if (w.first >= T) continue;  // no query sees this key tile: nothing to load
         const int kb = kvu % KB;
         if (kvu >= KB && !(ok = mbar_wait(&bar.kv_empty[kb], ((kvu / KB) - 1) & 1, wc))) break;
@@ -636,23 +661,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t id_t = idesc_bf16_f32(128, D, true, true);       // dV, dK (transposed A)
       constexpr uint32_t id_q = idesc_bf16_f32(128, D, false, true);      // dQ
       const uint32_t ps0 = smem_u32(smPS);
+      // P, dS: read M-major (the transposed A of dV, dK) and K-major (the A of dQ)
+      const uint64_t pt_desc = sdesc_sw128(ps0, L::kSubBytes, 1024);
+      const uint64_t pk_desc = sdesc_sw128(ps0, 16, 1024);
       bool ok = true;
       int git = 0, kvu = 0;
       int accu = 0;  // items whose dK, dV accumulators were used
       // S = Q K_j^T into the S columns (free once the previous P has been read out)
       auto issue_scores = [&](int stage, uint32_t k0) {
-        const uint32_t q_s = smem_u32(smQ + stage * L::kTileBytes);
+        const uint64_t qa = sdesc_sw128(smem_u32(smQ + stage * L::kTileBytes), 16, 1024);
+        const uint64_t kb = sdesc_sw128(k0, 16, 1024);
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
-          mma_bf16_ss(tmem + L::kColS, sdesc_sw128(q_s + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024), id_s,
-                      k > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + L::kColS, sdesc_adv(qa, off), sdesc_adv(kb, off), id_s, k > 0 ? 1u : 0u);
         }
         mma_commit(&bar.s_full);
       };
+      KvLenAhead kvl(blockIdx.x, gridDim.x, n_items, a);
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-        const BwdItem w = bwd_item(item, a);
+        const BwdItem w = bwd_item(item, kvl.next(item, a), a);
         if (w.first >= T) continue;
         const int kb = kvu % KB;
         const uint32_t k0 = smem_u32(smKV + kb * 2 * L::kTileBytes), v0 = k0 + L::kTileBytes;
@@ -666,14 +695,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int qt_next = next_query_tile(qt + 1, w.kt, w.kv_len, a.causal, a.block_mask, T);
           const int sq = git % QS, sd = git % DS;
           const uint32_t q0 = smem_u32(smQ + sq * L::kTileBytes), do0 = smem_u32(smDO + sd * L::kTileBytes);
+          const uint32_t psb = static_cast<uint32_t>(git & 1) * L::kPSBytes;
           // dP = dO_i V_j^T (when dQ shares dP's columns, the previous dQ must have been drained)
           if (!(ok = mbar_wait(&bar.do_full[sd], (git / DS) & 1, wc))) break;
           tc_fence_after();
+          {
+            const uint64_t da = sdesc_sw128(do0, 16, 1024), vb = sdesc_sw128(v0, 16, 1024);
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
-            mma_bf16_ss(tmem + L::kColDP, sdesc_sw128(do0 + off, 16, 1024), sdesc_sw128(v0 + off, 16, 1024), id_s,
-                        k > 0 ? 1u : 0u);
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
+              mma_bf16_ss(tmem + L::kColDP, sdesc_adv(da, off), sdesc_adv(vb, off), id_s, k > 0 ? 1u : 0u);
+            }
           }
           mma_commit(&bar.dp_full);
           // dV += P^T dO_i; the first of an item overwrites the accumulators, which the
@@ -683,8 +715,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k)
-            mma_bf16_ss(tmem + L::kColDV, sdesc_sw128(ps0 + k * 2048, L::kSubBytes, 1024),
-                        sdesc_sw128(do0 + k * 2048, L::kSubBytes, 1024), id_t, (itl > 0 || k > 0) ? 1u : 0u);
+            mma_bf16_ss(tmem + L::kColDV, sdesc_adv(pt_desc, psb + k * 2048), sdesc_adv(sdesc_sw128(do0, L::kSubBytes, 1024), k * 2048),
+                        id_t, (itl > 0 || k > 0) ? 1u : 0u);
           mma_commit(&bar.dv_done);
           mma_commit(&bar.do_empty[sd]);
           // next tile's scores: the S columns were read out before p_full
@@ -697,15 +729,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k)
-            mma_bf16_ss(tmem + L::kColDK, sdesc_sw128(ps0 + k * 2048, L::kSubBytes, 1024),
-                        sdesc_sw128(q0 + k * 2048, L::kSubBytes, 1024), id_t, (itl > 0 || k > 0) ? 1u : 0u);
+            mma_bf16_ss(tmem + L::kColDK, sdesc_adv(pt_desc, psb + k * 2048), sdesc_adv(sdesc_sw128(q0, L::kSubBytes, 1024), k * 2048),
+                        id_t, (itl > 0 || k > 0) ? 1u : 0u);
           if (git >= 1 && !(ok = mbar_wait(&bar.dq_free, (git - 1) & 1, wc))) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k)
-            mma_bf16_ss(tmem + L::kColDQ, sdesc_sw128(ps0 + (k / 4) * L::kSubBytes + (k % 4) * 32, 16, 1024),
-                        sdesc_sw128(k0 + k * 2048, L::kSubBytes, 1024), id_q, k > 0 ? 1u : 0u);
-          mma_commit(&bar.dkdq_done);
+            mma_bf16_ss(tmem + L::kColDQ, sdesc_adv(pk_desc, psb + (k / 4) * L::kSubBytes + (k % 4) * 32),
+                        sdesc_adv(sdesc_sw128(k0, L::kSubBytes, 1024), k * 2048), id_q, k > 0 ? 1u : 0u);
+          mma_commit(&bar.dkdq_done[git & 1]);
           mma_commit(&bar.q_empty[sq]);
           qt = qt_next;
         }
@@ -726,20 +758,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int r = wq * 32 + lane;  // query row (P, dS, dQ) or key row (dK, dV) inside the tile
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const float sl2 = a.scale_log2;
-    const uint32_t psrow = smem_u32(smPS) + hc * L::kSubBytes;
-    uint8_t* blk = smDQ + (hc * 4 + wq) * L::kStageBytes;  // this warp's 32x32 fp32 dQ staging block
-    uint8_t* stv = smem + L::kST;     // dV, dK staging
-    uint8_t* stk = stv + L::kTileBytes;
+    const uint32_t ps_half = smem_u32(smPS) + hc * L::kSubBytes;
+    uint8_t* blk = smDQ + (hc * 4 + wq) * L::kStageBytes;  // this warp's staging block (dQ, then dV | dK)
     bool ok = true;
     int git = 0;
     bool pending = false;  // dQ of iteration git-1 not yet drained
     int pend_qt = 0, pend_head = 0;
+    // LSE and D of query row `row` of head `head` (+inf and 0 past the last tile)
+    auto load_stats = [&](int head, int t, float& lse_v, float& d_v) {
+      const int row = t * kTile + r;
+      if (t < T && row < a.N) {
+        const size_t idx = static_cast<size_t>(head) * a.N + row;
+        lse_v = lse[idx];
+        d_v = dsum[idx];
+      } else {
+        lse_v = pos_inf();
+        d_v = 0.f;
+      }
+    };
     // dQ of query tile qt_d of head h_d (this warp's 32 rows x 32 columns): TMEM ->
     // swizzled shared block -> TMA reduce-add into the float32 accumulator
     auto drain_dq = [&](int qt_d, int h_d) {
       uint32_t t[32];
       tmem_ld32(tmem + lane_off + L::kColDQ + 32 * hc, t);
-      if (lane == 0) bulk_wait_read_all();  // the block's last reduce has read it
+      if (lane == 0) bulk_wait_read_all();  // the block's last bulk copy has read it
       __syncwarp();
       const uint32_t row = smem_u32(blk);
 #pragma unroll
@@ -755,35 +797,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_store_commit();
       }
     };
-    // Every warp walks every item and reaches both epilogue barriers even after a wait
-    // has given up (ok == false), so the named barriers always stay matched; an aborted
-    // CTA only skips the work.
+    // wait for the dK, dQ MMAs of iteration j (tile pair j completes dkdq_done[j % 2])
+    auto wait_dkdq = [&](int j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar.dkdq_done[j & 1], (j >> 1) & 1, wc));
+      return ok;
+    };
+    // The statistics of an item's first query tile are loaded one item ahead.
+    KvLenAhead kvl(blockIdx.x, gridDim.x, n_items, a);
+    float lse_c = pos_inf(), d_c = 0.f;
+    if (static_cast<int>(blockIdx.x) < n_items) {
+      const BwdItem w0 = bwd_item(blockIdx.x, kvl.peek(), a);
+      load_stats(w0.head, w0.first, lse_c, d_c);
+    }
+    // Every warp walks every item; an aborted CTA (ok == false) only skips the work.
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      const BwdItem w = bwd_item(item, a);
+      const BwdItem w = bwd_item(item, kvl.next(item, a), a);
       const bool work = w.first < T;
-      auto load_stats = [&](int t, float& lse_v, float& d_v) {
-        const int row = t * kTile + r;
-        if (t < T && row < a.N) {
-          const size_t idx = static_cast<size_t>(w.head) * a.N + row;
-          lse_v = lse[idx];
-          d_v = dsum[idx];
-        } else {
-          lse_v = pos_inf();
-          d_v = 0.f;
-        }
-      };
+      float lse_x = pos_inf(), d_x = 0.f;  // the next item's first tile, in flight during this item
+      if (item + static_cast<int>(gridDim.x) < n_items) {
+        const BwdItem wn = bwd_item(item + gridDim.x, kvl.peek(), a);
+        load_stats(wn.head, wn.first, lse_x, d_x);
+      }
       const int key0 = w.kt * kTile + 64 * hc;
-      float lse_r, d_r;
-      load_stats(w.first, lse_r, d_r);
+      float lse_r = lse_c, d_r = d_c;
       for (int qt = w.first; ok && qt < T; ++git) {
         const int qt_next = next_query_tile(qt + 1, w.kt, w.kv_len, a.causal, a.block_mask, T);
         float lse_n, d_n;
-        load_stats(qt_next, lse_n, d_n);
+        load_stats(w.head, qt_next, lse_n, d_n);
         const int q_row = qt * kTile + r;
         if (lse_r == -pos_inf()) lse_r = pos_inf();  // a row that sees no key contributes nothing
         const float lse2 = lse_r * kLog2e;
         const bool need_mask = (w.kt * kTile + kTile > w.kv_len) || (a.causal && w.kt == qt);
         const int lim = a.causal ? min(w.kv_len, q_row + 1) : w.kv_len;  // keys [kt*128, lim) visible
+        const uint32_t psrow = ps_half + static_cast<uint32_t>(git & 1) * L::kPSBytes;
 
         ok = mbar_wait(&bar.s_full, git & 1, wc);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -807,24 +853,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
         }
-        if (git >= 1) {
-          // the previous dK, dQ MMAs are done: dS_{i-1} is no longer read, and dQ_{i-1} is ready
-          ok = mbar_wait(&bar.dkdq_done, (git - 1) & 1, wc);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          if (pending) {
-            tc_fence_after();
-            drain_dq(pend_qt, pend_head);
-            tc_fence_before();
-            mbar_arrive(&bar.dq_free);
-            pending = false;
-          }
-        }
+        // this buffer last held dS of iteration git-2: its dK, dQ MMAs must be done
+        if (git >= 2 && !wait_dkdq(git - 2)) break;
 #pragma unroll
         for (int g = 0; g < 8; ++g)
           st_shared_v4(psrow + sw128_offset(r, g), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&bar.p_full);
+        // the previous dQ drains while the MMA warp runs dV and the next scores
+        if (pending) {
+          if (!wait_dkdq(git - 1)) break;
+          tc_fence_after();
+          drain_dq(pend_qt, pend_head);
+          tc_fence_before();
+          mbar_arrive(&bar.dq_free);
+          pending = false;
+        }
 
         ok = mbar_wait(&bar.dp_full, git & 1, wc);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -857,11 +902,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         lse_r = lse_n;
         d_r = d_n;
       }
-      // end of the item: its last dK, dQ MMAs (and so all its MMAs) complete with dkdq_done
-      if (ok && work) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar.dkdq_done, (git - 1) & 1, wc));
-      }
-      if (ok && work) {
+      lse_c = lse_x;
+      d_c = d_x;
+      // end of the item: its last dK, dQ MMAs (and so all its MMAs) are done
+      if (ok && work && wait_dkdq(git - 1)) {
         tc_fence_after();
         if (pending) {
           drain_dq(pend_qt, pend_head);
@@ -870,10 +914,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           pending = false;
         }
       }
-      // epilogue: this warpgroup's 32 columns of dV_j and scale * dK_j as bf16 into the
-      // staging tiles, then one TMA store of each; key tiles no query sees get zeros
-      if (warp == 2 && lane == 0) bulk_wait_read_all();  // the previous item's stores have read the staging
-      named_barrier(1, 256);
+      // epilogue: this warp's 32 key rows x 32 columns of dV_j and scale * dK_j as bf16,
+      // staged in its own block (64-byte rows, 64-byte swizzle) and stored by TMA; key
+      // tiles no query sees get zeros
+      uint32_t wv[16], wk[16];
       {
         uint32_t tv[32], tk[32];
         if (ok && work) {
@@ -886,24 +930,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) tv[i] = tk[i] = 0u;
         }
-        uint32_t wv[16], wk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           wv[i] = pack_bf16x2(__uint_as_float(tv[2 * i]), __uint_as_float(tv[2 * i + 1]));
           wk[i] = pack_bf16x2(__uint_as_float(tk[2 * i]) * a.scale, __uint_as_float(tk[2 * i + 1]) * a.scale);
         }
+      }
+      if (lane == 0) bulk_wait_read_all();  // the block's last bulk copy (a dQ reduce) has read it
+      __syncwarp();
+      const uint32_t sv = smem_u32(blk), sk = sv + 2048;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t off = sw128_offset(r, 4 * hc + q);
-          st_shared_v4(smem_u32(stv) + off, wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
-          st_shared_v4(smem_u32(stk) + off, wk[4 * q], wk[4 * q + 1], wk[4 * q + 2], wk[4 * q + 3]);
-        }
+      for (int q = 0; q < 4; ++q) {
+        st_shared_v4(sv + sw64_offset(lane, q), wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
+        st_shared_v4(sk + sw64_offset(lane, q), wk[4 * q], wk[4 * q + 1], wk[4 * q + 2], wk[4 * q + 3]);
       }
       fence_proxy_async_smem();
-      named_barrier(1, 256);
-      if (warp == 2 && lane == 0) {
-        tma_store_3d(&tm_dv, stv, 0, w.kt * kTile, w.head);
-        tma_store_3d(&tm_dk, stk, 0, w.kt * kTile, w.head);
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&tm_dv, blk, 32 * hc, w.kt * kTile + wq * 32, w.head);
+        tma_store_3d(&tm_dk, blk + 2048, 32 * hc, w.kt * kTile + wq * 32, w.head);
         tma_store_commit();
       }
     }
@@ -962,16 +1007,6 @@ __global__ void __launch_bounds__(256) bwd_postprocess_kernel(const float4* __re
   }
 }
 
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      n = 152;
-  }
-  return n;
-}
-
 unsigned grid_for(long long work, int per_block) {
   long long blocks = (work + per_block - 1) / per_block;
   const long long cap = static_cast<long long>(sm_count()) * 8;
@@ -986,17 +1021,15 @@ cudaError_t launch_bwd_main_d(const BwdMaps& m, const float* lse, const float* d
   if constexpr (D == 64) {
     // persistent: one CTA per SM walks the key tiles
     using L = PBwdLayout<D>;
-    cudaError_t e = cudaFuncSetAttribute(bwd_persistent_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::kSmemBytes);
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(bwd_persistent_kernel<D>), L::kSmemBytes);
     if (e != cudaSuccess) return e;
     const long long grid = n_items < sm_count() ? n_items : sm_count();
     bwd_persistent_kernel<D><<<static_cast<unsigned>(grid), kBwdThreads, L::kSmemBytes, stream>>>(
-        m.q, m.k, m.v, m.dout, m.dk, m.dv, m.dq_acc, lse, dsum, a);
+        m.q, m.k, m.v, m.dout, m.dk32, m.dv32, m.dq_acc, lse, dsum, a);
   } else {
     // one CTA per key tile
     using L = BwdLayout<D>;
-    cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::kSmemBytes);
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(bwd_main_kernel<D>), L::kSmemBytes);
     if (e != cudaSuccess) return e;
     bwd_main_kernel<D><<<static_cast<unsigned>(n_items), kBwdThreads, L::kSmemBytes, stream>>>(
         m.q, m.k, m.v, m.dout, m.dk, m.dv, m.dq_acc, lse, dsum, a);

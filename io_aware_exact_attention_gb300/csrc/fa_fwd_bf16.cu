@@ -71,6 +71,31 @@ struct FwdBarriers {
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
+// Maximum of a 128-value row: eight independent 3-input max chains of eight steps,
+// then a three-level tree (a two-chain loop is a 32-step latency chain).
+__device__ __forceinline__ float row_max128(const float (&v)[kTile]) {
+  float m[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = fmaxf(v[2 * k], v[2 * k + 1]);
+#pragma unroll
+  for (int c = 16; c < kTile; c += 16)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m[k] = fmax3(m[k], v[c + 2 * k], v[c + 2 * k + 1]);
+  return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], fmax3(m[5], m[6], m[7])));
+}
+
+// Sum of a 128-value row: eight independent accumulators (four paired adds per step).
+__device__ __forceinline__ float row_sum128(const float (&v)[kTile]) {
+  float a[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a[k] = v[k];
+#pragma unroll
+  for (int c = 8; c < kTile; c += 8)
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) fadd2(a[k], a[k + 1], v[c + k], v[c + k + 1]);
+  return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+}
+
 // Key tile kt is loaded when either query tile of the CTA sees it.
 __device__ __forceinline__ bool pair_sees(const int (&qt)[2], int kt, int kv_len, const AttnArgs& a) {
   if (tile_pair_visible(qt[0], kt, kv_len, a.causal, a.block_mask, a.n_tiles)) return true;
@@ -281,13 +306,7 @@ __global__ void __launch_bounds__(FwdLayout<D, NQ>::kThreads, FwdLayout<D, NQ>::
           for (int c = 0; c < kTile; ++c)
             if (key0 + c >= lim) s[c] = neg_inf();
         }
-        float mx0 = neg_inf(), mx1 = neg_inf();
-#pragma unroll
-        for (int c = 0; c < kTile; c += 4) {
-          mx0 = fmax3(mx0, s[c], s[c + 1]);
-          mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
-        }
-        const float mx = fmaxf(mx0, mx1) * sl2;
+        const float mx = row_max128(s) * sl2;
         const float m_new = (mx > m_run + kRescaleSlack) ? mx : m_run;
         const float m_use = (m_new == neg_inf()) ? 0.f : m_new;
         const float alpha = ex2(m_run - m_use);
@@ -299,16 +318,11 @@ __global__ void __launch_bounds__(FwdLayout<D, NQ>::kThreads, FwdLayout<D, NQ>::
           s[c] = ex2(s[c]);
           s[c + 1] = ex2(s[c + 1]);
         }
-        float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
-#pragma unroll
-        for (int c = 0; c < kTile; c += 4) {
-          fadd2(sum0, sum1, s[c], s[c + 1]);
-          fadd2(sum2, sum3, s[c + 2], s[c + 3]);
-        }
+        const float tile_sum = row_sum128(s);
         uint32_t pk[kTile / 2];
 #pragma unroll
         for (int c = 0; c < kTile; c += 2) pk[c / 2] = pack_bf16x2(s[c], s[c + 1]);
-        l_run = l_run * alpha + ((sum0 + sum1) + (sum2 + sum3));
+        l_run = l_run * alpha + tile_sum;
         m_run = m_new;
         // P replaces S in the tile's TMEM buffer (bf16 pairs, columns [0, 64))
         tmem_st32(t_s, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
@@ -382,11 +396,392 @@ __global__ void __launch_bounds__(FwdLayout<D, NQ>::kThreads, FwdLayout<D, NQ>::
   }
 }
 
+// Persistent forward for d = 64: two CTAs per SM, each walking (query tile, head) items
+// so that TMEM is allocated once per CTA and the next item's loads and first score MMA
+// overlap this item's epilogue.  P has TMEM columns of its own (S 128, P 64, O 64), so
+// the scores of the next key tile are computed while the softmax of this one runs: the
+// MMA warp issues S_{u+1} as soon as the softmax warps have read S_u out of TMEM.
+// K and V have rings of their own (a K stage is free once its score MMA is done, a V
+// stage once its P V is), and one producer lane streams K ahead of V while another
+// loads Q, so the next scores never wait on a V or Q load.  Q is double-buffered by
+// item; an item's Q buffer is the staging tile of its O.
+template <int D>
+struct PFwdLayout {
+  static_assert(D == 64, "the persistent forward is the d = 64 kernel");
+  static constexpr int kThreads = 192;  // producer warp, MMA warp, one softmax warpgroup
+  static constexpr int kStages = 2;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kSubBytes = kTile * 64 * 2;
+  static constexpr int kQ = 0;  // 2 Q buffers (item j in buffer j % 2)
+  static constexpr int kK = kQ + 2 * kTileBytes;
+  static constexpr int kV = kK + kStages * kTileBytes;
+  static constexpr int kEnd = kV + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kEnd + 1024;
+  static constexpr uint32_t kTmemCols = 256;
+  static constexpr uint32_t kColS = 0;    // scores, float32, 128 columns
+  static constexpr uint32_t kColP = 128;  // P as bf16 pairs, 64 columns
+  static constexpr uint32_t kColO = 192;  // output accumulator, 64 columns
+  static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
+};
+
+struct PFwdBarriers {
+  uint64_t q_full[2], q_empty[2];
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t s_full, s_free, p_full, o_done, o_free;
+  uint64_t drain;
+};
+
+// Item j of CTA c (rounds in snake order so that, with the heaviest items first,
+// every CTA gets a similar total); -1 once the CTA has no more items.
+__device__ __forceinline__ int pfwd_item(int j, int c, int G, int n_items) {
+  const int idx = j * G + ((j & 1) ? (G - 1 - c) : c);
+  return idx < n_items ? idx : -1;
+}
+
+struct FwdItem {
+  int qt, head, kv_len;
+};
+
+__device__ __forceinline__ FwdItem pfwd_decode(int idx, const AttnArgs& a) {
+  FwdItem w;
+  const int BH = a.B * a.H;
+  const int qi = idx / BH;
+  w.head = idx % BH;
+  w.qt = a.causal ? (a.n_tiles - 1 - qi) : qi;  // causal: longest rows first
+  w.kv_len = clamp_kv_len(a.kv_len, w.head / a.H, a.N);
+  return w;
+}
+
+// Position in a CTA's sequence of (item, visible key tile) pairs; j < 0 past the end.
+struct FwdCursor {
+  int j, kt;
+  bool first;  // the item's first key tile
+  FwdItem w;
+};
+
+// First pair at or after item j (items without a visible key tile are skipped).
+__device__ __forceinline__ FwdCursor pfwd_cursor_from(int j, int c, int G, int n_items, const AttnArgs& a) {
+  FwdCursor cur;
+  cur.first = true;
+  for (;; ++j) {
+    const int idx = pfwd_item(j, c, G, n_items);
+    if (idx < 0) {
+      cur.j = -1;
+      cur.kt = a.n_tiles;
+      return cur;
+    }
+    cur.w = pfwd_decode(idx, a);
+    cur.kt = next_key_tile(cur.w.qt, 0, cur.w.kv_len, a.causal, a.block_mask, a.n_tiles);
+    if (cur.kt < a.n_tiles) {
+      cur.j = j;
+      return cur;
+    }
+  }
+}
+
+__device__ __forceinline__ FwdCursor pfwd_cursor_next(const FwdCursor& cur, int c, int G, int n_items,
+                                                      const AttnArgs& a) {
+  FwdCursor nxt = cur;
+  nxt.kt = next_key_tile(cur.w.qt, cur.kt + 1, cur.w.kv_len, a.causal, a.block_mask, a.n_tiles);
+  nxt.first = false;
+  if (nxt.kt < a.n_tiles) return nxt;
+  return pfwd_cursor_from(cur.j + 1, c, G, n_items, a);
+}
+
+template <int D>
+__global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
+    fwd_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                          float* __restrict__ lse_out, const AttnArgs a) {
+  using L = PFwdLayout<D>;
+  constexpr int S = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) PFwdBarriers bar;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int T = a.n_tiles;
+  const int n_items = T * a.B * a.H;
+  const int G = gridDim.x, c = blockIdx.x;
+  const WaitCtx wc{&abort_flag, a.status};
+  uint8_t* smQ = smem + L::kQ;
+  uint8_t* smK = smem + L::kK;
+  uint8_t* smV = smem + L::kV;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.q_full[i], 1);
+      mbar_init(&bar.q_empty[i], 1);
+      mbar_init(&bar.k_full[i], 1);
+      mbar_init(&bar.k_empty[i], 1);
+      mbar_init(&bar.v_full[i], 1);
+      mbar_init(&bar.v_empty[i], 1);
+    }
+    mbar_init(&bar.s_full, 1);
+    mbar_init(&bar.s_free, 128);
+    mbar_init(&bar.p_full, 128);
+    mbar_init(&bar.o_done, 1);
+    mbar_init(&bar.o_free, 128);
+    mbar_init(&bar.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_s, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      // K and V of every (item, key tile) pair, K one pair ahead of V
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      int uk = 0, uv = 0;  // K, V ring uses
+      bool ok = true;
+      FwdCursor ck = pfwd_cursor_from(0, c, G, n_items, a);
+      FwdCursor cv = ck;
+      while (ok && cv.j >= 0) {
+        while (ok && ck.j >= 0 && uk <= uv + 1) {
+          const int s = uk % S;
+          if (uk >= S && !(ok = mbar_wait(&bar.k_empty[s], ((uk / S) - 1) & 1, wc))) break;
+          mbar_arrive_expect_tx(&bar.k_full[s], L::kTileBytes);
+          tma_load_3d(smK + s * L::kTileBytes, &tm_k, &bar.k_full[s], 0, ck.kt * kTile, ck.w.head);
+          ck = pfwd_cursor_next(ck, c, G, n_items, a);
+          ++uk;
+        }
+        if (!ok) break;
+        const int s = uv % S;
+        if (uv >= S && !(ok = mbar_wait(&bar.v_empty[s], ((uv / S) - 1) & 1, wc))) break;
+        mbar_arrive_expect_tx(&bar.v_full[s], L::kTileBytes);
+        tma_load_3d(smV + s * L::kTileBytes, &tm_v, &bar.v_full[s], 0, cv.kt * kTile, cv.w.head);
+        cv = pfwd_cursor_next(cv, c, G, n_items, a);
+        ++uv;
+      }
+      if (!ok) {
+        // let the loads already issued land before the CTA can exit
+        for (int i = (uk > S ? uk - S : 0); i < uk; ++i) mbar_drain(&bar.k_full[i % S], (i / S) & 1, 100000000ull);
+        for (int i = (uv > S ? uv - S : 0); i < uv; ++i) mbar_drain(&bar.v_full[i % S], (i / S) & 1, 100000000ull);
+      }
+    } else if (lane == 1) {
+      // Q of every item (the epilogue of item j - 2 frees its buffer)
+      tma_prefetch_desc(&tm_q);
+      int j = 0;
+      bool ok = true;
+      for (int idx; ok && (idx = pfwd_item(j, c, G, n_items)) >= 0; ++j) {
+        const FwdItem w = pfwd_decode(idx, a);
+        const int qb = j & 1;
+        if (j >= 2 && !(ok = mbar_wait(&bar.q_empty[qb], ((j >> 1) - 1) & 1, wc))) break;
+        mbar_arrive_expect_tx(&bar.q_full[qb], L::kTileBytes);
+        tma_load_3d(smQ + qb * L::kTileBytes, &tm_q, &bar.q_full[qb], 0, w.qt * kTile, w.head);
+      }
+      if (!ok)
+        for (int i = (j > 2 ? j - 2 : 0); i < j; ++i) mbar_drain(&bar.q_full[i & 1], (i >> 1) & 1, 100000000ull);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+      const uint64_t kdesc = sdesc_sw128(smem_u32(smK), 16, 1024);
+      const uint64_t vdesc = sdesc_sw128(smem_u32(smV), L::kSubBytes, 1024);
+      bool ok = true;
+      // S = Q K^T of pair `cur` from K/V stage `stage` into the S columns
+      auto issue_scores = [&](const FwdCursor& cur, int stage) {
+        const uint64_t qdesc = sdesc_sw128(smem_u32(smQ + (cur.j & 1) * L::kTileBytes), 16, 1024);
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_bf16_ss(tmem + L::kColS, sdesc_adv(qdesc, k * 32), sdesc_adv(kdesc, stage * L::kTileBytes + k * 32),
+                      idesc_s, k > 0 ? 1u : 0u);
+        mma_commit(&bar.s_full);
+        mma_commit(&bar.k_empty[stage]);
+      };
+      int u = 0;  // pairs so far (= S and P V products, = K/V ring uses)
+      FwdCursor cur = pfwd_cursor_from(0, c, G, n_items, a);
+      if (cur.j >= 0) {
+        ok = mbar_wait(&bar.q_full[cur.j & 1], (cur.j >> 1) & 1, wc) && mbar_wait(&bar.k_full[0], 0, wc);
+        if (ok) issue_scores(cur, 0);
+      }
+      // The next scores go out as soon as the softmax warps have read these out of TMEM:
+      // before this pair's P V inside an item, after it across items (the next item's Q
+      // may wait for this item's epilogue, which waits for this P V).
+      auto next_scores = [&](const FwdCursor& cur, const FwdCursor& nxt) -> bool {
+        if (nxt.j != cur.j && !mbar_wait(&bar.q_full[nxt.j & 1], (nxt.j >> 1) & 1, wc)) return false;
+        if (!mbar_wait(&bar.k_full[(u + 1) % S], ((u + 1) / S) & 1, wc)) return false;
+        if (!mbar_wait(&bar.s_free, u & 1, wc)) return false;
+        issue_scores(nxt, (u + 1) % S);
+        return true;
+      };
+      while (ok && cur.j >= 0) {
+        const FwdCursor nxt = pfwd_cursor_next(cur, c, G, n_items, a);
+        const int s = u % S;
+        if (nxt.j == cur.j && !(ok = next_scores(cur, nxt))) break;
+        // O (+)= P V; the first product of an item overwrites the accumulator, which the
+        // epilogue of the CTA's previous item must have read out
+        if (!(ok = mbar_wait(&bar.v_full[s], (u / S) & 1, wc))) break;
+        if (!(ok = mbar_wait(&bar.p_full, u & 1, wc))) break;
+        if (cur.first && cur.j >= 1 && !(ok = mbar_wait(&bar.o_free, (cur.j - 1) & 1, wc))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k)
+          mma_bf16_ts(tmem + L::kColO, tmem + L::kColP + k * 8, sdesc_adv(vdesc, s * L::kTileBytes + k * 2048),
+                      idesc_o, (!cur.first || k > 0) ? 1u : 0u);
+        mma_commit(&bar.o_done);
+        mma_commit(&bar.v_empty[s]);
+        if (nxt.j >= 0 && nxt.j != cur.j && !(ok = next_scores(cur, nxt))) break;
+        cur = nxt;
+        ++u;
+      }
+      if (!ok) {
+        mma_commit(&bar.drain);
+        mbar_drain(&bar.drain, 0, 100000000ull);
+      }
+    }
+  } else {
+    // --------------------------------------------------- softmax + epilogue (warps 2..5)
+    const int wq = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + L::kColS;
+    const uint32_t t_p = tmem + lane_off + L::kColP;
+    const uint32_t t_o = tmem + lane_off + L::kColO;
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    int u = 0;  // pairs so far, over all items
+    // Every warp walks every item and reaches the epilogue barrier once per item, also
+    // after a wait has given up (ok == false), so the named barrier stays matched.
+    for (int j = 0, idx; (idx = pfwd_item(j, c, G, n_items)) >= 0; ++j) {
+      const FwdItem w = pfwd_decode(idx, a);
+      const int qb = j & 1;
+      const int q_row = w.qt * kTile + r;
+      float m_run = neg_inf();  // max used for the exponentials, log2 domain (scale * log2 e applied)
+      float l_run = 0.f;        // running sum of exp2(s - m_run)
+      int n = 0;                // key tiles of this item
+      for (int kt = next_key_tile(w.qt, 0, w.kv_len, a.causal, a.block_mask, T); ok && kt < T;
+           kt = next_key_tile(w.qt, kt + 1, w.kv_len, a.causal, a.block_mask, T), ++n, ++u) {
+        ok = mbar_wait(&bar.s_full, u & 1, wc);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        float sv[kTile];
+        {
+          uint32_t t[kTile];
+          tmem_ld128(t_s, t);
+#pragma unroll
+          for (int i = 0; i < kTile; ++i) sv[i] = __uint_as_float(t[i]);
+        }
+        tc_fence_before();
+        mbar_arrive(&bar.s_free);  // the MMA warp may overwrite S with the next scores
+        // element mask: key padding tail, causal diagonal (the N tail is covered by kv_len <= N)
+        const int key0 = kt * kTile;
+        if (key0 + kTile > w.kv_len || (a.causal && kt == w.qt)) {
+          const int lim = a.causal ? min(w.kv_len, q_row + 1) : w.kv_len;  // keys [key0, lim) visible
+#pragma unroll
+          for (int cc = 0; cc < kTile; ++cc)
+            if (key0 + cc >= lim) sv[cc] = neg_inf();
+        }
+        const float mx = row_max128(sv) * sl2;
+        const float m_new = (mx > m_run + kRescaleSlack) ? mx : m_run;
+        const float m_use = (m_new == neg_inf()) ? 0.f : m_new;
+        const float alpha = ex2(m_run - m_use);
+#pragma unroll
+        for (int cc = 0; cc < kTile; cc += 2) {
+          ffma2(sv[cc], sv[cc + 1], sv[cc], sv[cc + 1], sl2, -m_use);
+          sv[cc] = ex2(sv[cc]);
+          sv[cc + 1] = ex2(sv[cc + 1]);
+        }
+        const float tile_sum = row_sum128(sv);
+        uint32_t pk[kTile / 2];
+#pragma unroll
+        for (int cc = 0; cc < kTile; cc += 2) pk[cc / 2] = pack_bf16x2(sv[cc], sv[cc + 1]);
+        l_run = l_run * alpha + tile_sum;
+        m_run = m_new;
+        // the previous P V has read P and updated O
+        if (u > 0) {
+          ok = mbar_wait(&bar.o_done, (u - 1) & 1, wc);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+        }
+        tmem_st64(t_p, pk);
+        if (n > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t t[32];
+            tmem_ld32(t_o + c0, t);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
+            tmem_st32(t_o + c0, t);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bar.p_full);
+      }
+
+      // epilogue: O = O_acc / l (bf16) staged in this item's Q buffer and stored by TMA; LSE = m + ln l
+      bool have_o = ok && n > 0;
+      if (have_o) {
+        ok = mbar_wait(&bar.o_done, (u - 1) & 1, wc);  // this item's last P V
+        have_o = __all_sync(0xffffffffu, ok);
+        ok = have_o;
+        tc_fence_after();
+      }
+      uint32_t wo[D / 2];
+      {
+        const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+        uint32_t t[D];
+        if (have_o) {
+          tmem_ld64(t_o, t);
+        } else {
+#pragma unroll
+          for (int i = 0; i < D; ++i) t[i] = 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < D / 2; ++i)
+          wo[i] = pack_bf16x2(__uint_as_float(t[2 * i]) * inv_l, __uint_as_float(t[2 * i + 1]) * inv_l);
+      }
+      tc_fence_before();
+      mbar_arrive(&bar.o_free);  // the accumulator may be overwritten by the next item
+      // the Q tile has landed (an item without keys never waited for it) and no MMA reads it any more
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_full[qb], (j >> 1) & 1, wc));
+      const uint32_t orow = smem_u32(smQ + qb * L::kTileBytes);
+#pragma unroll
+      for (int q = 0; q < D / 8; ++q)
+        st_shared_v4(orow + sw128_offset(r, q), wo[4 * q], wo[4 * q + 1], wo[4 * q + 2], wo[4 * q + 3]);
+      fence_proxy_async_smem();
+      named_barrier(1, 128);
+      if (wq == 2 && lane == 0) {
+        tma_store_3d(&tm_o, smQ + qb * L::kTileBytes, 0, w.qt * kTile, w.head);
+        tma_store_commit();
+        bulk_wait_read_all();
+        mbar_arrive(&bar.q_empty[qb]);  // the staging tile has been read: the producer may load Q of item j + 2
+      }
+      if (q_row < a.N) {
+        const float lse = (n > 0 && l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : neg_inf();
+        lse_out[static_cast<size_t>(w.head) * a.N + q_row] = lse;
+      }
+    }
+    if (wq == 2 && lane == 0) tma_store_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
 template <int D, int NQ>
 cudaError_t launch_fwd_d(const FwdMaps& maps, float* lse, const AttnArgs& a, cudaStream_t stream) {
   using L = FwdLayout<D, NQ>;
-  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       L::kSmemBytes);
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fwd_bf16_kernel<D, NQ>), L::kSmemBytes);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>((a.n_tiles + NQ - 1) / NQ) * a.B * a.H;
   fwd_bf16_kernel<D, NQ><<<static_cast<unsigned>(grid), L::kThreads, L::kSmemBytes, stream>>>(maps.q, maps.k, maps.v,
@@ -397,7 +792,17 @@ cudaError_t launch_fwd_d(const FwdMaps& maps, float* lse, const AttnArgs& a, cud
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const FwdMaps& maps, float* lse, const AttnArgs& a, cudaStream_t stream) {
-  return a.d == 64 ? launch_fwd_d<64, 1>(maps, lse, a, stream) : launch_fwd_d<128, 2>(maps, lse, a, stream);
+  if (a.d == 128) return launch_fwd_d<128, 2>(maps, lse, a, stream);
+  // d = 64: persistent, two CTAs per SM
+  using L = PFwdLayout<64>;
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fwd_persistent_kernel<64>), L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long n_items = static_cast<long long>(a.n_tiles) * a.B * a.H;
+  const long long slots = 2LL * sm_count();
+  const long long grid = n_items < slots ? n_items : slots;
+  fwd_persistent_kernel<64><<<static_cast<unsigned>(grid), L::kThreads, L::kSmemBytes, stream>>>(
+      maps.q, maps.k, maps.v, maps.o, lse, a);
+  return cudaGetLastError();
 }
 
 }  // namespace fa

@@ -30,7 +30,15 @@ struct FwdMaps {
 struct BwdMaps {
   CUtensorMap q, k, v, dout, dk, dv;
   CUtensorMap dq_acc;  // float32 [B*H, N, d], 32 x 32 boxes, 128-byte swizzle (reduce-add target)
+  CUtensorMap dk32, dv32;  // dK, dV again with 32 x 32 boxes and 64-byte swizzle (one warp's block)
 };
+
+// Streaming multiprocessors of the current device (cached after the first call).
+int sm_count();
+
+// Raises a kernel's dynamic shared memory limit to `bytes` once per (kernel, device), so
+// that repeated launches (and launches under stream capture) make no attribute call.
+cudaError_t ensure_smem_limit(const void* kernel, int bytes);
 
 cudaError_t launch_fwd_bf16(const FwdMaps& maps, float* lse, const AttnArgs& a, cudaStream_t stream);
 
