@@ -6,10 +6,11 @@ One step = one pass of the whole attention path over one batch of the workload:
 fa_fwd (one kernel) then fa_bwd's three stages (preprocess, main, postprocess),
 inputs resident in HBM.  Each timed step calls the API (--graphs instead captures
 each stage's call once as a CUDA graph after the warm-up and replays the graphs).
-Timed with CUDA events on the launching stream between the
-stages, L2 flushed between timed steps (512 MiB written, then 256 MiB read so that
-the flush's own dirty lines are written back before the next step), max over ranks.  Prints
-one JSON line (rank 0).
+Timed with CUDA events on the launching stream around each step; a second,
+shorter pass puts an event between the stages for the per-kernel times.  L2 is
+flushed between timed steps (512 MiB written, then 256 MiB read so that the
+flush's own dirty lines are written back before the next step).  Max over ranks;
+rank 0 prints one JSON line.
 
 FLOP convention: forward 4*B*H*N^2*d (halved when causal), backward 2.5x forward;
 `value` is forward+backward TFLOP/s.  The roofline object reports the dominant
@@ -269,7 +270,9 @@ def time_workload(name, steps, warmup, torch, fa, flush, dist=None, sampler=None
         for _ in range(2):
             flush()
             step()
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    # Timed steps: one event pair around each step.  The four launches of a step run
+    # back to back, so each kernel's launch overlaps the tail of the one before it.
+    step_events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     if dist is not None and dist.is_initialized():
         dist.barrier()
     torch.cuda.synchronize()
@@ -278,9 +281,19 @@ def time_workload(name, steps, warmup, torch, fa, flush, dist=None, sampler=None
         t0 = time.perf_counter()
         for i in range(steps):
             flush()
-            step(events[i])
+            step_events[i][0].record(stream)
+            step()
+            step_events[i][1].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
+    # Stage breakdown: a shorter pass with an event between the stages (which
+    # serialises them), for the per-kernel times and the roofline.
+    n_stage = max(3, min(steps, 100))
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_stage)]
+    for i in range(n_stage):
+        flush()
+        step(events[i])
+    torch.cuda.synchronize()
     if dist is not None and dist.is_initialized():
         dist.barrier()
     if fa.fa_get_device_status() != 0:
@@ -290,8 +303,9 @@ def time_workload(name, steps, warmup, torch, fa, flush, dist=None, sampler=None
     for ev in events:
         for j, key in enumerate(keys):
             stage[key] += ev[j].elapsed_time(ev[j + 1])
-    ms = {k2: v2 / steps for k2, v2 in stage.items()}
-    ms["step"] = sum(ms.values())
+    ms = {k2: v2 / n_stage for k2, v2 in stage.items()}
+    ms["stages_sum"] = sum(ms.values())
+    ms["step"] = sum(ev[0].elapsed_time(ev[1]) for ev in step_events) / steps
     ms["wall_s"] = wall
     ms["launch"] = launch_mode
     pairs = visited_tile_pairs(N, causal, inp.kv_len, inp.block_mask, B, H)

@@ -94,6 +94,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse,
                     const float* __restrict__ dsum, const AttnArgs a) {
   using L = BwdLayout<D>;
+  griddep_launch_dependents();
+  griddep_wait();  // every global access of this kernel comes after the previous kernel of the stream
   constexpr int QS = L::kQStages;
   constexpr int DS = L::kDoStages;
   extern __shared__ uint8_t smem_raw[];
@@ -555,6 +557,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse,
                     const float* __restrict__ dsum, const AttnArgs a) {
   using L = PBwdLayout<D>;
+  griddep_launch_dependents();
+  griddep_wait();  // every global access of this kernel comes after the previous kernel of the stream
   constexpr int QS = L::kQStages;
   constexpr int DS = L::kDoStages;
   constexpr int KB = L::kKvBuffers;
@@ -969,6 +973,8 @@ template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
                                                              float* __restrict__ dsum, float4* __restrict__ dq_acc,
                                                              long long rows) {
+  griddep_launch_dependents();
+  griddep_wait();
   constexpr int kLanesPerRow = D / 8;
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -999,6 +1005,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint4* __rest
 // dq (bf16) = dq_acc (float32), eight elements per thread.
 __global__ void __launch_bounds__(256) bwd_postprocess_kernel(const float4* __restrict__ dq_acc,
                                                               uint4* __restrict__ dq, long long n8) {
+  griddep_launch_dependents();
+  griddep_wait();
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long e = tid; e < n8; e += nthreads) {
@@ -1024,17 +1032,16 @@ cudaError_t launch_bwd_main_d(const BwdMaps& m, const float* lse, const float* d
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(bwd_persistent_kernel<D>), L::kSmemBytes);
     if (e != cudaSuccess) return e;
     const long long grid = n_items < sm_count() ? n_items : sm_count();
-    bwd_persistent_kernel<D><<<static_cast<unsigned>(grid), kBwdThreads, L::kSmemBytes, stream>>>(
-        m.q, m.k, m.v, m.dout, m.dk32, m.dv32, m.dq_acc, lse, dsum, a);
+    return launch_pdl(bwd_persistent_kernel<D>, static_cast<unsigned>(grid), kBwdThreads, L::kSmemBytes, stream, m.q,
+                      m.k, m.v, m.dout, m.dk32, m.dv32, m.dq_acc, lse, dsum, a);
   } else {
     // one CTA per key tile
     using L = BwdLayout<D>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(bwd_main_kernel<D>), L::kSmemBytes);
     if (e != cudaSuccess) return e;
-    bwd_main_kernel<D><<<static_cast<unsigned>(n_items), kBwdThreads, L::kSmemBytes, stream>>>(
-        m.q, m.k, m.v, m.dout, m.dk, m.dv, m.dq_acc, lse, dsum, a);
+    return launch_pdl(bwd_main_kernel<D>, static_cast<unsigned>(n_items), kBwdThreads, L::kSmemBytes, stream, m.q, m.k,
+                      m.v, m.dout, m.dk, m.dv, m.dq_acc, lse, dsum, a);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace
@@ -1043,13 +1050,11 @@ cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* dsum, 
                                   cudaStream_t stream) {
   const long long rows = static_cast<long long>(a.B) * a.H * a.N;
   const unsigned grid = grid_for(rows * (a.d / 8), 256);
-  if (a.d == 64)
-    bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout),
-                                                        dsum, reinterpret_cast<float4*>(dq_acc), rows);
-  else
-    bwd_preprocess_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout),
-                                                         dsum, reinterpret_cast<float4*>(dq_acc), rows);
-  return cudaGetLastError();
+  const uint4* o4 = static_cast<const uint4*>(o);
+  const uint4* do4 = static_cast<const uint4*>(dout);
+  float4* acc = reinterpret_cast<float4*>(dq_acc);
+  if (a.d == 64) return launch_pdl(bwd_preprocess_kernel<64>, grid, 256, 0, stream, o4, do4, dsum, acc, rows);
+  return launch_pdl(bwd_preprocess_kernel<128>, grid, 256, 0, stream, o4, do4, dsum, acc, rows);
 }
 
 cudaError_t launch_bwd_main_bf16(const BwdMaps& maps, const float* lse, const float* dsum, const AttnArgs& a,
@@ -1059,9 +1064,8 @@ cudaError_t launch_bwd_main_bf16(const BwdMaps& maps, const float* lse, const fl
 
 cudaError_t launch_bwd_postprocess(const float* dq_acc, void* dq, const AttnArgs& a, cudaStream_t stream) {
   const long long n8 = static_cast<long long>(a.B) * a.H * a.N * a.d / 8;
-  bwd_postprocess_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
-                                                                static_cast<uint4*>(dq), n8);
-  return cudaGetLastError();
+  return launch_pdl(bwd_postprocess_kernel, grid_for(n8, 256), 256, 0, stream, reinterpret_cast<const float4*>(dq_acc),
+                    static_cast<uint4*>(dq), n8);
 }
 
 }  // namespace fa

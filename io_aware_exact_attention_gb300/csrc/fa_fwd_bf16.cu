@@ -113,6 +113,8 @@ __global__ void __launch_bounds__(FwdLayout<D, NQ>::kThreads, FwdLayout<D, NQ>::
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     float* __restrict__ lse_out, const AttnArgs a) {
   using L = FwdLayout<D, NQ>;
+  griddep_launch_dependents();
+  griddep_wait();  // every global access of this kernel comes after the previous kernel of the stream
   constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -494,6 +496,8 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                           float* __restrict__ lse_out, const AttnArgs a) {
   using L = PFwdLayout<D>;
+  griddep_launch_dependents();
+  griddep_wait();  // every global access of this kernel comes after the previous kernel of the stream
   constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -784,9 +788,8 @@ cudaError_t launch_fwd_d(const FwdMaps& maps, float* lse, const AttnArgs& a, cud
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fwd_bf16_kernel<D, NQ>), L::kSmemBytes);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>((a.n_tiles + NQ - 1) / NQ) * a.B * a.H;
-  fwd_bf16_kernel<D, NQ><<<static_cast<unsigned>(grid), L::kThreads, L::kSmemBytes, stream>>>(maps.q, maps.k, maps.v,
-                                                                                             maps.o, lse, a);
-  return cudaGetLastError();
+  return launch_pdl(fwd_bf16_kernel<D, NQ>, static_cast<unsigned>(grid), L::kThreads, L::kSmemBytes, stream, maps.q,
+                    maps.k, maps.v, maps.o, lse, a);
 }
 
 }  // namespace
@@ -800,9 +803,8 @@ cudaError_t launch_fwd_bf16(const FwdMaps& maps, float* lse, const AttnArgs& a, 
   const long long n_items = static_cast<long long>(a.n_tiles) * a.B * a.H;
   const long long slots = 2LL * sm_count();
   const long long grid = n_items < slots ? n_items : slots;
-  fwd_persistent_kernel<64><<<static_cast<unsigned>(grid), L::kThreads, L::kSmemBytes, stream>>>(
-      maps.q, maps.k, maps.v, maps.o, lse, a);
-  return cudaGetLastError();
+  return launch_pdl(fwd_persistent_kernel<64>, static_cast<unsigned>(grid), L::kThreads, L::kSmemBytes, stream, maps.q,
+                    maps.k, maps.v, maps.o, lse, a);
 }
 
 }  // namespace fa

@@ -33,6 +33,25 @@ struct BwdMaps {
   CUtensorMap dk32, dv32;  // dK, dV again with 32 x 32 boxes and 64-byte swizzle (one warp's block)
 };
 
+// Launches `kernel` on `stream` with programmatic stream serialization, so that its CTAs
+// may be scheduled while the previous kernel of the stream finishes (each kernel calls
+// griddep_wait before touching global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Streaming multiprocessors of the current device (cached after the first call).
 int sm_count();
 

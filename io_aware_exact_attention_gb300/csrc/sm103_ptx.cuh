@@ -137,6 +137,14 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Programmatic dependent launch.  launch_dependents lets the next kernel of the stream
+// (launched with programmatic stream serialization) start launching its CTAs once every
+// CTA of this grid has executed it; griddep_wait blocks until the kernels this grid
+// depends on have completed and their memory operations are visible.  A kernel launched
+// without the attribute returns from griddep_wait at once.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Wait until every bulk copy this thread committed has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
