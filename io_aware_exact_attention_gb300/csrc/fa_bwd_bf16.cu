@@ -36,10 +36,15 @@ namespace {
 constexpr int kBwdThreads = 320;
 constexpr float kLog2e = 1.44269504088896340736f;
 
+// d = 128, one CTA per key tile.  TMEM: S and dP take turns in one 128-column region
+// (S is read out before dP is written, dP before the next S), which leaves dV, dK and
+// dQ 128 columns each, so the dQ drain (warps 6..9) only has to finish before the next
+// dQ and never holds up the next dP.  Warps 2..5 compute P and dS.
 template <int D>
 struct BwdLayout {
+  static_assert(D == 128, "the one-CTA-per-key-tile backward is the d = 128 kernel");
   static constexpr int kQStages = 2;
-  static constexpr int kDoStages = D == 64 ? 2 : 1;
+  static constexpr int kDoStages = 1;
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kSubBytes = kTile * 64 * 2;
   static constexpr int kStageBytes = 32 * 32 * 4;  // one 32x32 fp32 dQ block
@@ -48,18 +53,16 @@ struct BwdLayout {
   static constexpr int kQ = kV + kTileBytes;
   static constexpr int kDO = kQ + kQStages * kTileBytes;
   static constexpr int kPS = kDO + kDoStages * kTileBytes;   // P, then dS, of the current tile pair
-  static constexpr int kDQ = kPS + kTile * kTile * 2;        // 4 warps x 2 buffers of 32x32 fp32
+  static constexpr int kDQ = kPS + kTile * kTile * 2;        // 4 drain warps x 2 buffers of 32x32 fp32
   static constexpr int kEnd = kDQ + 4 * 2 * kStageBytes;
   static constexpr int kSmemBytes = kEnd + 1024;
-  // TMEM columns.  At d = 128 the dQ tile lives in dP's columns (dP is consumed before dQ is formed).
-  static constexpr uint32_t kColS = 0;
-  static constexpr uint32_t kColDP = 128;
-  static constexpr uint32_t kColDV = 256;
-  static constexpr uint32_t kColDK = 256 + D;
-  static constexpr bool kDqAliasesDP = (256 + 3 * D) > 512;
-  static constexpr uint32_t kColDQ = kDqAliasesDP ? kColDP : static_cast<uint32_t>(256 + 2 * D);
+  static constexpr uint32_t kColSP = 0;  // S, then dP, of the current tile pair
+  static constexpr uint32_t kColDV = 128;
+  static constexpr uint32_t kColDK = 128 + D;
+  static constexpr uint32_t kColDQ = 128 + 2 * D;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kComputeArrivals = 128u;
+  static constexpr uint32_t kComputeArrivals = 128u;  // one warpgroup per role
+  static_assert(kColDQ + D <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -70,7 +73,7 @@ struct BwdBarriers {
   uint64_t q_empty[BwdLayout<D>::kQStages];
   uint64_t do_full[BwdLayout<D>::kDoStages];
   uint64_t do_empty[BwdLayout<D>::kDoStages];
-  uint64_t s_full, dp_full, p_full, dv_done, ds_full, dkdq_done, dq_free, drain;
+  uint64_t s_full, s_free, dp_full, dp_free, p_full, dv_done, ds_full, dq_free, dkdq_done, drain;
 };
 
 __device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000); }
@@ -133,12 +136,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bar.do_empty[s], 1);
     }
     mbar_init(&bar.s_full, 1);
+    mbar_init(&bar.s_free, L::kComputeArrivals);
     mbar_init(&bar.dp_full, 1);
+    mbar_init(&bar.dp_free, L::kComputeArrivals);
     mbar_init(&bar.p_full, L::kComputeArrivals);
     mbar_init(&bar.dv_done, 1);
     mbar_init(&bar.ds_full, L::kComputeArrivals);
-    mbar_init(&bar.dkdq_done, 1);
     mbar_init(&bar.dq_free, L::kComputeArrivals);
+    mbar_init(&bar.dkdq_done, 1);
     mbar_init(&bar.drain, 1);
     fence_mbar_init();
   }
@@ -189,18 +194,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);   // S, dP
       constexpr uint32_t id_t = idesc_bf16_f32(128, D, true, true);       // dV, dK (transposed A)
       constexpr uint32_t id_q = idesc_bf16_f32(128, D, false, true);      // dQ
-      const uint32_t k0 = smem_u32(smK), v0 = smem_u32(smV), ps0 = smem_u32(smPS);
+      const uint64_t kd = sdesc_sw128(smem_u32(smK), 16, 1024);          // K, K-major (S)
+      const uint64_t kn = sdesc_sw128(smem_u32(smK), L::kSubBytes, 1024);  // K, N-major (dQ)
+      const uint64_t vd = sdesc_sw128(smem_u32(smV), 16, 1024);          // V, K-major (dP)
+      const uint64_t pt = sdesc_sw128(smem_u32(smPS), L::kSubBytes, 1024);  // P, dS read M-major (dV, dK)
+      const uint64_t pk = sdesc_sw128(smem_u32(smPS), 16, 1024);           // dS read K-major (dQ)
       bool ok = true;
       int it = 0;
-      // S = Q_i K_j^T into the S columns (free once the previous P has been read out)
+      // S = Q_i K_j^T into the S/dP columns
       auto issue_scores = [&](int stage) {
-        const uint32_t q_s = smem_u32(smQ + stage * L::kTileBytes);
+        const uint64_t qd = sdesc_sw128(smem_u32(smQ + stage * L::kTileBytes), 16, 1024);
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
-          mma_bf16_ss(tmem + L::kColS, sdesc_sw128(q_s + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024), id_s,
-                      k > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + L::kColSP, sdesc_adv(qd, off), sdesc_adv(kd, off), id_s, k > 0 ? 1u : 0u);
         }
         mma_commit(&bar.s_full);
       };
@@ -209,21 +217,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok) issue_scores(0);
       }
       if (ok) {
-        // Per query tile: dP, dV, then the next tile's scores (so the P/dS warps can
-        // move straight on to the next tile), then dK and dQ.
+        // Per query tile: dP (once S is read out), dV, the next S (once dP is read
+        // out), dK, then dQ (once the previous dQ is drained).
         for (int qt = first; qt < T; ++it) {
           const int qt_next = next_query_tile(qt + 1, kt, kv_len, a.causal, a.block_mask, T);
           const int sq = it % QS, sd = it % DS;
-          const uint32_t q0 = smem_u32(smQ + sq * L::kTileBytes), do0 = smem_u32(smDO + sd * L::kTileBytes);
-          // dP = dO_i V_j^T (when dQ shares dP's columns, the previous dQ must have been drained)
+          const uint64_t qn = sdesc_sw128(smem_u32(smQ + sq * L::kTileBytes), L::kSubBytes, 1024);
+          const uint64_t dod = sdesc_sw128(smem_u32(smDO + sd * L::kTileBytes), 16, 1024);
+          const uint64_t don = sdesc_sw128(smem_u32(smDO + sd * L::kTileBytes), L::kSubBytes, 1024);
+          // dP = dO_i V_j^T
           if (!(ok = mbar_wait(&bar.do_full[sd], (it / DS) & 1, wc))) break;
-          if (L::kDqAliasesDP && it >= 1 && !(ok = mbar_wait(&bar.dq_free, (it - 1) & 1, wc))) break;
+          if (!(ok = mbar_wait(&bar.s_free, it & 1, wc))) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
-            mma_bf16_ss(tmem + L::kColDP, sdesc_sw128(do0 + off, 16, 1024), sdesc_sw128(v0 + off, 16, 1024), id_s,
-                        k > 0 ? 1u : 0u);
+            mma_bf16_ss(tmem + L::kColSP, sdesc_adv(dod, off), sdesc_adv(vd, off), id_s, k > 0 ? 1u : 0u);
           }
           mma_commit(&bar.dp_full);
           // dV += P^T dO_i
@@ -231,30 +240,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k)
-            mma_bf16_ss(tmem + L::kColDV, sdesc_sw128(ps0 + k * 2048, L::kSubBytes, 1024),
-                        sdesc_sw128(do0 + k * 2048, L::kSubBytes, 1024), id_t, (it > 0 || k > 0) ? 1u : 0u);
+            mma_bf16_ss(tmem + L::kColDV, sdesc_adv(pt, k * 2048), sdesc_adv(don, k * 2048), id_t,
+                        (it > 0 || k > 0) ? 1u : 0u);
           mma_commit(&bar.dv_done);
           mma_commit(&bar.do_empty[sd]);
-          // next tile's scores: the S columns were read out before p_full
+          // the next scores
           if (qt_next < T) {
             if (!(ok = mbar_wait(&bar.q_full[(it + 1) % QS], ((it + 1) / QS) & 1, wc))) break;
+            if (!(ok = mbar_wait(&bar.dp_free, it & 1, wc))) break;
             issue_scores((it + 1) % QS);
           }
-          // dK += dS^T Q_i ; dQ_i = dS K_j
+          // dK += dS^T Q_i (the last reader of Q_i)
           if (!(ok = mbar_wait(&bar.ds_full, it & 1, wc))) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k)
-            mma_bf16_ss(tmem + L::kColDK, sdesc_sw128(ps0 + k * 2048, L::kSubBytes, 1024),
-                        sdesc_sw128(q0 + k * 2048, L::kSubBytes, 1024), id_t, (it > 0 || k > 0) ? 1u : 0u);
-          if (!L::kDqAliasesDP && it >= 1 && !(ok = mbar_wait(&bar.dq_free, (it - 1) & 1, wc))) break;
+            mma_bf16_ss(tmem + L::kColDK, sdesc_adv(pt, k * 2048), sdesc_adv(qn, k * 2048), id_t,
+                        (it > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bar.q_empty[sq]);
+          // dQ_i = dS K_j
+          if (it >= 1 && !(ok = mbar_wait(&bar.dq_free, (it - 1) & 1, wc))) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kTile / 16; ++k)
-            mma_bf16_ss(tmem + L::kColDQ, sdesc_sw128(ps0 + (k / 4) * L::kSubBytes + (k % 4) * 32, 16, 1024),
-                        sdesc_sw128(k0 + k * 2048, L::kSubBytes, 1024), id_q, k > 0 ? 1u : 0u);
-          mma_commit(&bar.dkdq_done);
-          mma_commit(&bar.q_empty[sq]);
+            mma_bf16_ss(tmem + L::kColDQ, sdesc_adv(pk, (k / 4) * L::kSubBytes + (k % 4) * 32),
+                        sdesc_adv(kn, k * 2048), id_q, k > 0 ? 1u : 0u);
+          mma_commit(&bar.dkdq_done);  // dS is no longer read, dQ_i is complete
           qt = qt_next;
         }
       }
@@ -298,6 +309,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool need_mask = (key0 + kTile > kv_len) || (a.causal && kt == qt);
       const int lim = a.causal ? min(kv_len, q_row + 1) : kv_len;  // keys [key0, lim) visible
 
+      // P = exp2(S scale log2e - LSE log2e), one 64-column half at a time; the MMA warp
+      // may write dP over S once both halves are in registers
       ok = mbar_wait(&bar.s_full, it & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -305,8 +318,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int c0 = 0; c0 < kTile; c0 += 64) {
         uint32_t t[64];
-        tmem_ld64(tmem + lane_off + L::kColS + c0, t);
-        // all exponentials of the chunk first (independent), then the mask and the packing
+        tmem_ld64(tmem + lane_off + L::kColSP + c0, t);
+        if (c0 == 64) {
+          tc_fence_before();
+          mbar_arrive(&bar.s_free);
+        }
         float f[64];
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
@@ -334,15 +350,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       mbar_arrive(&bar.p_full);
 
+      // dS = P * (dP - D), one 64-column half at a time.  dS replaces P in the shared
+      // buffer once the dV MMA has read P (waited before the first half is written);
+      // the MMA warp may write the next S over dP once the second half is loaded (the
+      // pipe is still busy with dV until about then).
       ok = mbar_wait(&bar.dp_full, it & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      // dS replaces P in the shared buffer once the dV MMA has read P: the first
-      // 64-column half is formed first, then written after that wait.
 #pragma unroll
       for (int c0 = 0; c0 < kTile; c0 += 64) {
         uint32_t t[64];
-        tmem_ld64(tmem + lane_off + L::kColDP + c0, t);
+        tmem_ld64(tmem + lane_off + L::kColSP + c0, t);
+        if (c0 == 64) {
+          tc_fence_before();
+          mbar_arrive(&bar.dp_free);
+        }
         float f[64];
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
@@ -379,7 +401,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int it = 0;
     int nblk = 0;
     for (int qt = first; qt < T; qt = next_query_tile(qt + 1, kt, kv_len, a.causal, a.block_mask, T), ++it) {
-      // dQ_i partial = dS K_j in TMEM: scale it and add it into the float32 accumulator
+      // dQ_i = dS K_j in its own TMEM columns: scale it and add it into the float32
+      // accumulator; it only has to be drained before dQ_{i+1} is formed
       ok = mbar_wait(&bar.dkdq_done, it & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -413,8 +436,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) tma_store_wait_all();
 
     // epilogue: dV_j and scale * dK_j as bf16 through shared memory (the two Q
-    // stages, idle now) and TMA.  Every MMA has completed: the last dkdq_done was
-    // waited above and follows all earlier MMAs.
+    // stages: the last dK, which the final dkdq_done follows, was their last reader)
+    // and TMA
     const bool have = ok && it > 0;
     tc_fence_after();
     uint8_t* stv = smQ;

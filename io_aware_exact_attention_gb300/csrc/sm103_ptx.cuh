@@ -366,6 +366,10 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a 128-byte-swizzled
 // tile whose rows are 128 bytes apart (the layout TMA writes for SWIZZLE_128B).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
