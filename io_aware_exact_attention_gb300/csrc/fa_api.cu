@@ -230,6 +230,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   if (!encode_bf16(&maps.q, q, BH, N, d) || !encode_bf16(&maps.k, k, BH, N, d) || !encode_bf16(&maps.v, v, BH, N, d) ||
       !encode_bf16(&maps.o, o, BH, N, d))
     return FA_ERR_CUDA;
+  maps.o_ptr = o;
   return launch_status(fa::launch_fwd_bf16(maps, lse, a, s));
 }
 

@@ -407,6 +407,11 @@ __global__ void __launch_bounds__(FwdLayout<D, NQ>::kThreads, FwdLayout<D, NQ>::
 // stage once its P V is), and one producer lane streams K ahead of V while another
 // loads Q, so the next scores never wait on a V or Q load.  Q is double-buffered by
 // item; an item's Q buffer is the staging tile of its O.
+//
+// The per-item barriers (q_full, q_empty, o_free) count only items with at least one
+// visible key tile, in every role: with items skipped by one role but counted by
+// another, a parity wait could see a phase two completions away.  An item without a
+// visible key writes its zero rows of O with plain stores and touches no barrier.
 template <int D>
 struct PFwdLayout {
   static_assert(D == 64, "the persistent forward is the d = 64 kernel");
@@ -457,14 +462,17 @@ __device__ __forceinline__ FwdItem pfwd_decode(int idx, const AttnArgs& a) {
 // Position in a CTA's sequence of (item, visible key tile) pairs; j < 0 past the end.
 struct FwdCursor {
   int j, kt;
+  int k;       // index of the item among the CTA's items with a visible key tile
   bool first;  // the item's first key tile
   FwdItem w;
 };
 
-// First pair at or after item j (items without a visible key tile are skipped).
-__device__ __forceinline__ FwdCursor pfwd_cursor_from(int j, int c, int G, int n_items, const AttnArgs& a) {
+// First pair at or after item j, whose item is the k-th with a visible key tile
+// (items without one are skipped).
+__device__ __forceinline__ FwdCursor pfwd_cursor_from(int j, int k, int c, int G, int n_items, const AttnArgs& a) {
   FwdCursor cur;
   cur.first = true;
+  cur.k = k;
   for (;; ++j) {
     const int idx = pfwd_item(j, c, G, n_items);
     if (idx < 0) {
@@ -487,14 +495,14 @@ __device__ __forceinline__ FwdCursor pfwd_cursor_next(const FwdCursor& cur, int 
   nxt.kt = next_key_tile(cur.w.qt, cur.kt + 1, cur.w.kv_len, a.causal, a.block_mask, a.n_tiles);
   nxt.first = false;
   if (nxt.kt < a.n_tiles) return nxt;
-  return pfwd_cursor_from(cur.j + 1, c, G, n_items, a);
+  return pfwd_cursor_from(cur.j + 1, cur.k + 1, c, G, n_items, a);
 }
 
 template <int D>
 __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
     fwd_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                          float* __restrict__ lse_out, const AttnArgs a) {
+                          uint16_t* __restrict__ o_out, float* __restrict__ lse_out, const AttnArgs a) {
   using L = PFwdLayout<D>;
   griddep_launch_dependents();
   griddep_wait();  // every global access of this kernel comes after the previous kernel of the stream
@@ -550,7 +558,7 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
       tma_prefetch_desc(&tm_v);
       int uk = 0, uv = 0;  // K, V ring uses
       bool ok = true;
-      FwdCursor ck = pfwd_cursor_from(0, c, G, n_items, a);
+      FwdCursor ck = pfwd_cursor_from(0, 0, c, G, n_items, a);
       FwdCursor cv = ck;
       while (ok && cv.j >= 0) {
         while (ok && ck.j >= 0 && uk <= uv + 1) {
@@ -575,19 +583,22 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
         for (int i = (uv > S ? uv - S : 0); i < uv; ++i) mbar_drain(&bar.v_full[i % S], (i / S) & 1, 100000000ull);
       }
     } else if (lane == 1) {
-      // Q of every item (the epilogue of item j - 2 frees its buffer)
+      // Q of every item with a visible key tile; the k-th goes to buffer k % 2, which
+      // the epilogue of the (k-2)-th frees
       tma_prefetch_desc(&tm_q);
-      int j = 0;
+      int k = 0;
       bool ok = true;
-      for (int idx; ok && (idx = pfwd_item(j, c, G, n_items)) >= 0; ++j) {
+      for (int j = 0, idx; ok && (idx = pfwd_item(j, c, G, n_items)) >= 0; ++j) {
         const FwdItem w = pfwd_decode(idx, a);
-        const int qb = j & 1;
-        if (j >= 2 && !(ok = mbar_wait(&bar.q_empty[qb], ((j >> 1) - 1) & 1, wc))) break;
+        if (next_key_tile(w.qt, 0, w.kv_len, a.causal, a.block_mask, T) >= T) continue;
+        const int qb = k & 1;
+        if (k >= 2 && !(ok = mbar_wait(&bar.q_empty[qb], ((k >> 1) - 1) & 1, wc))) break;
         mbar_arrive_expect_tx(&bar.q_full[qb], L::kTileBytes);
         tma_load_3d(smQ + qb * L::kTileBytes, &tm_q, &bar.q_full[qb], 0, w.qt * kTile, w.head);
+        ++k;
       }
       if (!ok)
-        for (int i = (j > 2 ? j - 2 : 0); i < j; ++i) mbar_drain(&bar.q_full[i & 1], (i >> 1) & 1, 100000000ull);
+        for (int i = (k > 2 ? k - 2 : 0); i < k; ++i) mbar_drain(&bar.q_full[i & 1], (i >> 1) & 1, 100000000ull);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
@@ -599,7 +610,7 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
       bool ok = true;
       // S = Q K^T of pair `cur` from K/V stage `stage` into the S columns
       auto issue_scores = [&](const FwdCursor& cur, int stage) {
-        const uint64_t qdesc = sdesc_sw128(smem_u32(smQ + (cur.j & 1) * L::kTileBytes), 16, 1024);
+        const uint64_t qdesc = sdesc_sw128(smem_u32(smQ + (cur.k & 1) * L::kTileBytes), 16, 1024);
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
@@ -609,16 +620,16 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
         mma_commit(&bar.k_empty[stage]);
       };
       int u = 0;  // pairs so far (= S and P V products, = K/V ring uses)
-      FwdCursor cur = pfwd_cursor_from(0, c, G, n_items, a);
+      FwdCursor cur = pfwd_cursor_from(0, 0, c, G, n_items, a);
       if (cur.j >= 0) {
-        ok = mbar_wait(&bar.q_full[cur.j & 1], (cur.j >> 1) & 1, wc) && mbar_wait(&bar.k_full[0], 0, wc);
+        ok = mbar_wait(&bar.q_full[0], 0, wc) && mbar_wait(&bar.k_full[0], 0, wc);
         if (ok) issue_scores(cur, 0);
       }
       // The next scores go out as soon as the softmax warps have read these out of TMEM:
       // before this pair's P V inside an item, after it across items (the next item's Q
       // may wait for this item's epilogue, which waits for this P V).
       auto next_scores = [&](const FwdCursor& cur, const FwdCursor& nxt) -> bool {
-        if (nxt.j != cur.j && !mbar_wait(&bar.q_full[nxt.j & 1], (nxt.j >> 1) & 1, wc)) return false;
+        if (nxt.j != cur.j && !mbar_wait(&bar.q_full[nxt.k & 1], (nxt.k >> 1) & 1, wc)) return false;
         if (!mbar_wait(&bar.k_full[(u + 1) % S], ((u + 1) / S) & 1, wc)) return false;
         if (!mbar_wait(&bar.s_free, u & 1, wc)) return false;
         issue_scores(nxt, (u + 1) % S);
@@ -629,10 +640,10 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
         const int s = u % S;
         if (nxt.j == cur.j && !(ok = next_scores(cur, nxt))) break;
         // O (+)= P V; the first product of an item overwrites the accumulator, which the
-        // epilogue of the CTA's previous item must have read out
+        // epilogue of the CTA's previous item with a visible key tile must have read out
         if (!(ok = mbar_wait(&bar.v_full[s], (u / S) & 1, wc))) break;
         if (!(ok = mbar_wait(&bar.p_full, u & 1, wc))) break;
-        if (cur.first && cur.j >= 1 && !(ok = mbar_wait(&bar.o_free, (cur.j - 1) & 1, wc))) break;
+        if (cur.first && cur.k >= 1 && !(ok = mbar_wait(&bar.o_free, (cur.k - 1) & 1, wc))) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < kTile / 16; ++k)
@@ -660,12 +671,24 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
     const float sl2 = a.scale_log2;
     bool ok = true;
     int u = 0;  // pairs so far, over all items
-    // Every warp walks every item and reaches the epilogue barrier once per item, also
-    // after a wait has given up (ok == false), so the named barrier stays matched.
+    int k = 0;  // items with a visible key tile so far
+    // Every warp walks every item; an item with a visible key tile reaches the epilogue
+    // barrier once, also after a wait has given up (ok == false), so the named barrier
+    // stays matched.
     for (int j = 0, idx; (idx = pfwd_item(j, c, G, n_items)) >= 0; ++j) {
       const FwdItem w = pfwd_decode(idx, a);
-      const int qb = j & 1;
       const int q_row = w.qt * kTile + r;
+      if (next_key_tile(w.qt, 0, w.kv_len, a.causal, a.block_mask, T) >= T) {
+        // no key visible: O = 0 and LSE = -inf, by plain stores; no barrier involved
+        if (q_row < a.N) {
+          uint4* orow = reinterpret_cast<uint4*>(o_out + (static_cast<size_t>(w.head) * a.N + q_row) * D);
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(0u, 0u, 0u, 0u);
+          lse_out[static_cast<size_t>(w.head) * a.N + q_row] = neg_inf();
+        }
+        continue;
+      }
+      const int qb = k & 1;
       float m_run = neg_inf();  // max used for the exponentials, log2 domain (scale * log2 e applied)
       float l_run = 0.f;        // running sum of exp2(s - m_run)
       int n = 0;                // key tiles of this item
@@ -751,9 +774,9 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
           wo[i] = pack_bf16x2(__uint_as_float(t[2 * i]) * inv_l, __uint_as_float(t[2 * i + 1]) * inv_l);
       }
       tc_fence_before();
-      mbar_arrive(&bar.o_free);  // the accumulator may be overwritten by the next item
-      // the Q tile has landed (an item without keys never waited for it) and no MMA reads it any more
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_full[qb], (j >> 1) & 1, wc));
+      mbar_arrive(&bar.o_free);  // the accumulator may be overwritten by the next item with a visible key
+      // the Q tile has landed and no MMA reads it any more
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_full[qb], (k >> 1) & 1, wc));
       const uint32_t orow = smem_u32(smQ + qb * L::kTileBytes);
 #pragma unroll
       for (int q = 0; q < D / 8; ++q)
@@ -764,12 +787,13 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
         tma_store_3d(&tm_o, smQ + qb * L::kTileBytes, 0, w.qt * kTile, w.head);
         tma_store_commit();
         bulk_wait_read_all();
-        mbar_arrive(&bar.q_empty[qb]);  // the staging tile has been read: the producer may load Q of item j + 2
+        mbar_arrive(&bar.q_empty[qb]);  // the staging tile has been read: the producer may load the Q two items on
       }
       if (q_row < a.N) {
         const float lse = (n > 0 && l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : neg_inf();
         lse_out[static_cast<size_t>(w.head) * a.N + q_row] = lse;
       }
+      ++k;
     }
     if (wq == 2 && lane == 0) tma_store_wait_all();
   }
@@ -804,7 +828,7 @@ cudaError_t launch_fwd_bf16(const FwdMaps& maps, float* lse, const AttnArgs& a, 
   const long long slots = 2LL * sm_count();
   const long long grid = n_items < slots ? n_items : slots;
   return launch_pdl(fwd_persistent_kernel<64>, static_cast<unsigned>(grid), L::kThreads, L::kSmemBytes, stream, maps.q,
-                    maps.k, maps.v, maps.o, lse, a);
+                    maps.k, maps.v, maps.o, static_cast<uint16_t*>(maps.o_ptr), lse, a);
 }
 
 }  // namespace fa

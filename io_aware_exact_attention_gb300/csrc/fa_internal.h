@@ -25,6 +25,7 @@ struct AttnArgs {
 // Tensor maps for [B*H, N, d] bf16 tensors, boxes of 64 x 128 with 128-byte swizzle.
 struct FwdMaps {
   CUtensorMap q, k, v, o;
+  void* o_ptr;  // O itself, for rows written with plain stores
 };
 
 struct BwdMaps {
