@@ -53,3 +53,41 @@ def test_many_items_per_cta_with_empty_heads(causal):
         parity.check_forward(got["o"], lse[b, hh].cpu().numpy().astype(np.float64), ref["o"][b, hh],
                              ref["lse"][b, hh], what=f"head {b},{hh}")
         parity.check_grads(got, {n: ref[n][b, hh] for n in ("dq", "dk", "dv")}, what=f"head {b},{hh}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_items_per_cta_block_mask_with_empty_rows_and_columns(causal):
+    B, H, N, d = 16, 8, 1024, 64  # 1024 items in each direction, several per persistent CTA
+    inp = inputs.make_inputs(B, H, N, d, seed=5151 + int(causal), causal=causal,
+                             block_mask=dict(band=1, global_cols=0, frac=0.15))
+    T = N // 128
+    inp.block_mask[2, :] = 0      # query tile 2 sees nothing: O = 0, LSE = -inf on its rows
+    inp.block_mask[5, :] = 0
+    inp.block_mask[:, 6] = 0      # key tile 6 is seen by no query: dK = dV = 0 on its rows
+    inp.block_mask[:, 3] = 0
+    q, k, v, do = (parity.to_device(inp, n) for n in ("q", "k", "v", "dout"))
+    bm, kl = parity.masks_to_device(inp)
+    o, lse = fa.attention_forward(q, k, v, inp.scale, causal, bm, kl)
+    dq, dk, dv = fa.attention_backward(q, k, v, o, lse, do, inp.scale, causal, bm, kl)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == 0
+
+    for qt in (2, 5):
+        rows = slice(qt * 128, (qt + 1) * 128)
+        assert torch.count_nonzero(o[:, :, rows]) == 0
+        assert bool(torch.all(lse[:, :, rows] == float("-inf")))
+        assert torch.count_nonzero(dq[:, :, rows]) == 0
+    for kt in (3, 6):
+        rows = slice(kt * 128, (kt + 1) * 128)
+        assert torch.count_nonzero(dk[:, :, rows]) == 0 and torch.count_nonzero(dv[:, :, rows]) == 0
+
+    heads = [(0, 0), (5, 3), (11, 6), (15, 7)]
+    ref = oracle.attention_backward(inp.q, inp.k, inp.v, inp.dout, inp.scale, causal=causal,
+                                    block_mask=inp.block_mask, heads=heads)
+    h = parity.to_host64
+    for b, hh in heads:
+        got = {"o": h(o[b, hh]), "dq": h(dq[b, hh]), "dk": h(dk[b, hh]), "dv": h(dv[b, hh])}
+        parity.check_forward(got["o"], lse[b, hh].cpu().numpy().astype(np.float64), ref["o"][b, hh],
+                             ref["lse"][b, hh], what=f"head {b},{hh}")
+        parity.check_grads(got, {n: ref[n][b, hh] for n in ("dq", "dk", "dv")}, what=f"head {b},{hh}")
+    assert T == 8
