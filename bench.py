@@ -320,49 +320,88 @@ class _Null:
         return False
 
 
-def e2e_throughput(inp, steps, torch, fa):
-    """Same fwd+bwd through the public API from pinned host buffers; copies in the timed region."""
+def e2e_throughput(inp, steps, torch, fa, depth=2):
+    """The same fwd+bwd through the API (fa_fwd, fa_bwd) from pinned host buffers,
+    with every step's host->device copy of Q, K, V, dO (and the masks) and its
+    device->host copy of O, LSE, dQ, dK, dV inside the timed region.
+
+    The steps form a pipeline over `depth` sets of device buffers: step i+1's inputs
+    upload while step i computes and step i-1's results download, on three streams.
+    A set is reused only after the step before it has finished computing on it and
+    its results are on the host."""
     B, H, N, d = inp.q.shape
-    spec_causal = inp.causal
+    causal = inp.causal
     host = {n: torch.from_numpy(np.ascontiguousarray(inp.device_array(n)).view(np.int16)).view(torch.bfloat16)
             .pin_memory() for n in ("q", "k", "v", "dout")}
     host_kl = torch.from_numpy(inp.kv_len).pin_memory() if inp.kv_len is not None else None
     host_bm = torch.from_numpy(inp.block_mask).pin_memory() if inp.block_mask is not None else None
-    dev = {n: torch.empty(host[n].shape, dtype=torch.bfloat16, device="cuda") for n in host}
-    kl = torch.empty_like(host_kl, device="cuda") if host_kl is not None else None
-    bm = torch.empty_like(host_bm, device="cuda") if host_bm is not None else None
-    outs_host = {n: torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory() for n in ("o", "dq", "dk", "dv")}
-    lse_host = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-    ws = fa.new_workspace(dev["q"])
-    stream = torch.cuda.current_stream()
+    sets = []
+    for _ in range(depth):
+        dev = {n: torch.empty(host[n].shape, dtype=torch.bfloat16, device="cuda") for n in host}
+        sets.append({
+            "in": dev,
+            "kl": torch.empty_like(host_kl, device="cuda") if host_kl is not None else None,
+            "bm": torch.empty_like(host_bm, device="cuda") if host_bm is not None else None,
+            "out": {n: torch.empty((B, H, N, d), dtype=torch.bfloat16, device="cuda") for n in ("o", "dq", "dk", "dv")},
+            "lse": torch.empty((B, H, N), dtype=torch.float32, device="cuda"),
+            "ws": fa.new_workspace(dev["q"]),
+            "host_out": {n: torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory()
+                         for n in ("o", "dq", "dk", "dv")},
+            "host_lse": torch.empty((B, H, N), dtype=torch.float32).pin_memory(),
+            "ev": [torch.cuda.Event() for _ in range(3)],  # inputs on device, computed, results on host
+            "used": False,
+        })
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     h2d += (host_kl.numel() * 4 if host_kl is not None else 0) + (host_bm.numel() if host_bm is not None else 0)
-    d2h = sum(t.numel() * t.element_size() for t in outs_host.values()) + lse_host.numel() * 4
+    d2h = 4 * B * H * N * d * 2 + B * H * N * 4
 
-    def one():
-        for n in host:
-            dev[n].copy_(host[n], non_blocking=True)
-        if kl is not None:
-            kl.copy_(host_kl, non_blocking=True)
-        if bm is not None:
-            bm.copy_(host_bm, non_blocking=True)
-        o, lse = fa.attention_forward(dev["q"], dev["k"], dev["v"], inp.scale, spec_causal, bm, kl, stream)
-        dq, dk, dv = fa.attention_backward(dev["q"], dev["k"], dev["v"], o, lse, dev["dout"], inp.scale, spec_causal,
-                                           bm, kl, ws, stream)
-        for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
-            outs_host[n].copy_(t, non_blocking=True)
-        lse_host.copy_(lse, non_blocking=True)
+    def one(i):
+        st = sets[i % depth]
+        ev_in, ev_comp, ev_out = st["ev"]
+        if st["used"]:
+            s_in.wait_event(ev_comp)  # the step before on this set has read its inputs
+        with torch.cuda.stream(s_in):
+            for n in host:
+                st["in"][n].copy_(host[n], non_blocking=True)
+            if st["kl"] is not None:
+                st["kl"].copy_(host_kl, non_blocking=True)
+            if st["bm"] is not None:
+                st["bm"].copy_(host_bm, non_blocking=True)
+            ev_in.record(s_in)
+        s_comp.wait_event(ev_in)
+        if st["used"]:
+            s_comp.wait_event(ev_out)  # its previous results are on the host
+        q, k, v, do = (st["in"][n] for n in ("q", "k", "v", "dout"))
+        out = st["out"]
+        fa.fa_fwd(q, k, v, out["o"], st["lse"], inp.scale, causal, st["bm"], st["kl"], s_comp)
+        fa.fa_bwd(q, k, v, out["o"], st["lse"], do, out["dq"], out["dk"], out["dv"], st["ws"], inp.scale, causal,
+                  st["bm"], st["kl"], s_comp)
+        ev_comp.record(s_comp)
+        s_out.wait_event(ev_comp)
+        with torch.cuda.stream(s_out):
+            for n in ("o", "dq", "dk", "dv"):
+                st["host_out"][n].copy_(out[n], non_blocking=True)
+            st["host_lse"].copy_(st["lse"], non_blocking=True)
+            ev_out.record(s_out)
+        st["used"] = True
 
-    for _ in range(3):
-        one()
+    for i in range(3):
+        one(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        one()
-    e1.record(stream)
+    e0.record(s_in)
+    for s in (s_comp, s_out):
+        s.wait_event(e0)
+    for i in range(3, 3 + steps):
+        one(i)
+    for s in (s_comp, s_out):
+        s_in.wait_stream(s)
+    e1.record(s_in)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
+    if fa.fa_get_device_status() != 0:
+        raise RuntimeError("device status reports a timed-out wait")
     return ms, h2d, d2h
 
 
