@@ -290,8 +290,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int row = t * kTile + r;
       if (t < T && row < a.N) {
         const size_t idx = static_cast<size_t>(head) * a.N + row;
-        lse_v = lse[idx];
-        d_v = dsum[idx];
+        lse_v = ld_global_pinned(lse + idx);
+        d_v = ld_global_pinned(dsum + idx);
       } else {
         lse_v = pos_inf();
         d_v = 0.f;
@@ -554,7 +554,7 @@ __device__ __forceinline__ BwdItem bwd_item(int item, int kv_len_raw, const Attn
 // Key-padding length of item `item`'s batch (N without padding or past the last item).
 __device__ __forceinline__ int item_kv_len(int item, int n_items, const AttnArgs& a) {
   if (a.kv_len == nullptr || item >= n_items) return a.N;
-  return a.kv_len[(item % (a.B * a.H)) / a.H];
+  return ld_global_pinned(a.kv_len + (item % (a.B * a.H)) / a.H);
 }
 
 // kv_len of a CTA's items two items ahead: next() returns the current item's value and
@@ -796,8 +796,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int row = t * kTile + r;
       if (t < T && row < a.N) {
         const size_t idx = static_cast<size_t>(head) * a.N + row;
-        lse_v = lse[idx];
-        d_v = dsum[idx];
+        lse_v = ld_global_pinned(lse + idx);
+        d_v = ld_global_pinned(dsum + idx);
       } else {
         lse_v = pos_inf();
         d_v = 0.f;
