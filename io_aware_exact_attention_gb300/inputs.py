@@ -9,6 +9,10 @@ Recipe (one numpy ``default_rng`` stream per tensor, spawned from one seed):
   * Q, K, V, dO ~ N(0, 1), drawn in float32, then rounded to bf16 with
     round-to-nearest-even (kept exact as float32 for the oracle, and as raw bf16
     bits for the device);
+  * for the FP8 forward: the same float32 draws of Q, K, V, each divided by a
+    power-of-two per-tensor scale (the smallest with max|x| / scale <= 448) and
+    rounded to OCP FP8 E4M3 with round-to-nearest-even; the oracle gets
+    code value * scale, which is exact;
   * key-padding lengths: integers uniform on [lo, hi], one per sequence;
   * block mask over 128x128 tiles: a local band of +-band tiles, the first tile
     column (global tokens) and a fraction of tiles drawn uniformly without
@@ -46,6 +50,44 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
 def round_bf16(x: np.ndarray) -> np.ndarray:
     """Round float32 values to the nearest bf16 value, returned as float32."""
     return bf16_bits_to_f32(bf16_bits(x))
+
+
+E4M3_MAX = 448.0  # largest finite OCP FP8 E4M3 value (1.75 * 2^8); code 0x7F is NaN
+
+
+def e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> OCP FP8 E4M3 codes (uint8: sign, 4 exponent bits with bias 7, 3
+    mantissa bits), round to nearest even.  Magnitudes below 2^-6 use the subnormal
+    step 2^-9.  Raises ValueError for NaN and for values that round past 448."""
+    x = np.asarray(x, dtype=np.float32)
+    if np.isnan(x).any():
+        raise ValueError("NaN has no place in an E4M3 input")
+    a = np.abs(x).astype(np.float64)
+    _, e2 = np.frexp(a)                       # a = f * 2^e2 with f in [0.5, 1)
+    e = np.maximum(e2 - 1, -6)                # binade exponent, clamped to the subnormal range
+    q = np.rint(a / np.exp2(e - 3))           # exact division by a power of two; rint is ties-to-even
+    code = np.where(a < 2.0 ** -6, np.rint(a / 2.0 ** -9), (e + 7) * 8 + (q - 8))
+    if (code > 0x7E).any():
+        raise ValueError("value beyond the E4M3 range (|x| rounds above 448)")
+    return (code.astype(np.uint8) | np.where(np.signbit(x), 0x80, 0).astype(np.uint8)).astype(np.uint8)
+
+
+def e4m3_bits_to_f32(codes: np.ndarray) -> np.ndarray:
+    """OCP FP8 E4M3 codes -> exactly equal float32 values (0x7F / 0xFF decode to NaN)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int32)
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, m * 2.0 ** -9, (8.0 + m) * np.exp2(e - 10.0))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return np.where(c & 0x80, -mag, mag).astype(np.float32)
+
+
+def pow2_scale(x: np.ndarray) -> float:
+    """Smallest power of two s with max|x| / s <= 448 (1.0 for an all-zero tensor)."""
+    amax = float(np.max(np.abs(x))) if x.size else 0.0
+    if amax == 0.0:
+        return 1.0
+    return float(2.0 ** math.ceil(math.log2(amax / E4M3_MAX)))
 
 
 def _streams(seed: int, n: int):
@@ -141,6 +183,66 @@ WORKLOAD_SEEDS = {
     "tiny_fp32": 1001, "bert_large_padded": 1002, "gpt2_causal": 1003,
     "long_causal_16k": 1004, "long_causal_64k": 1004, "block_sparse_8k": 1005,
 }
+
+
+@dataclass
+class Fp8Inputs:
+    """Host copies of one FP8 forward workload.
+
+    q8, k8: E4M3 codes [B, H, N, d]; vt8: E4M3 codes of V transposed, [B, H, d, ldv]
+    (key index fastest, row stride ldv >= N a multiple of 16, columns past N zero).
+    q, k, v: float32 [B, H, N, d] holding code value * descale exactly -- the values
+    the oracle receives."""
+    q8: np.ndarray
+    k8: np.ndarray
+    vt8: np.ndarray
+    ldv: int
+    descale_q: float
+    descale_k: float
+    descale_v: float
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    scale: float
+    causal: bool
+    kv_len: np.ndarray | None
+    block_mask: np.ndarray | None
+    seed: int
+
+
+def quantize_e4m3(x: np.ndarray) -> tuple[np.ndarray, float, np.ndarray]:
+    """Per-tensor power-of-two scaling then E4M3 rounding: (codes, descale, x_q) with
+    x_q = codes' values * descale (exact float32)."""
+    s = pow2_scale(x)
+    codes = e4m3_bits(np.asarray(x, np.float32) / np.float32(s))
+    return codes, s, (e4m3_bits_to_f32(codes) * np.float32(s)).astype(np.float32)
+
+
+def make_fp8_inputs(B: int, H: int, N: int, d: int, *, seed: int, scale: float | None = None,
+                    causal: bool = False, kv_len_range: tuple[int, int] | None = None,
+                    block_mask: dict | None = None) -> Fp8Inputs:
+    """Q, K, V ~ N(0,1) (the float32 draws of make_inputs with the same seed), the same
+    masks, quantized to E4M3 with one power-of-two scale per tensor."""
+    raw = make_inputs(B, H, N, d, seed=seed, dtype="fp32", scale=scale, causal=causal,
+                      kv_len_range=kv_len_range, block_mask=block_mask, with_dout=False)
+    q8, sq, q = quantize_e4m3(raw.q)
+    k8, sk, k = quantize_e4m3(raw.k)
+    v8, sv, v = quantize_e4m3(raw.v)
+    ldv = max(16, (N + 15) // 16 * 16)
+    vt8 = np.zeros((B, H, d, ldv), np.uint8)
+    vt8[..., :N] = np.swapaxes(v8, 2, 3)
+    return Fp8Inputs(q8=q8, k8=k8, vt8=vt8, ldv=ldv, descale_q=sq, descale_k=sk, descale_v=sv, q=q, k=k, v=v,
+                     scale=raw.scale, causal=causal, kv_len=raw.kv_len, block_mask=raw.block_mask, seed=seed)
+
+
+def workload_fp8_inputs(name: str, *, seed: int | None = None, **override) -> Fp8Inputs:
+    """FP8 inputs of a named workload (its shape, masks and scale; optionally with
+    B/H/N overridden)."""
+    spec = dict(WORKLOADS[name])
+    for key in ("fwd_only", "dtype"):
+        spec.pop(key, None)
+    spec.update(override)
+    return make_fp8_inputs(seed=WORKLOAD_SEEDS[name] if seed is None else seed, **spec)
 
 
 def workload_inputs(name: str, *, seed: int | None = None, **override) -> AttentionInputs:
