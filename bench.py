@@ -106,7 +106,7 @@ def load_peaks():
 
 def kernel_source_digest(kernel):
     import hashlib
-    src = {"bwd_main": "fa_bwd_bf16.cu", "fwd": "fa_fwd_bf16.cu"}.get(kernel)
+    src = {"bwd_main": "fa_bwd_bf16.cu", "fwd": "fa_fwd.cu", "fwd_fp8": "fa_fwd.cu"}.get(kernel)
     if src is None:
         return None
     h = hashlib.sha256()
@@ -312,6 +312,39 @@ def time_workload(name, steps, warmup, torch, fa, flush, dist=None, sampler=None
     return inp, ms, pairs, (q, k, v, do, bm, kl)
 
 
+def time_fp8_forward(name, steps, warmup, torch, fa, flush):
+    """fa_fwd_fp8 on the E4M3 version of a workload (one launch per step, L2 flushed
+    between steps, one event pair per step on the launching stream).  Returns
+    (inputs, mean ms per launch)."""
+    inp = inputs.workload_fp8_inputs(name)
+    B, H, N, d = inp.q8.shape
+    dev = {n: torch.from_numpy(np.ascontiguousarray(getattr(inp, n))).cuda() for n in ("q8", "k8", "vt8")}
+    bm = torch.from_numpy(inp.block_mask).cuda() if inp.block_mask is not None else None
+    kl = torch.from_numpy(inp.kv_len).cuda() if inp.kv_len is not None else None
+    o = torch.empty((B, H, N, d), device="cuda", dtype=torch.bfloat16)
+    lse = torch.empty((B, H, N), device="cuda", dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+
+    def run():
+        fa.fa_fwd_fp8(dev["q8"], dev["k8"], dev["vt8"], o, lse, inp.scale, inp.descale_q, inp.descale_k,
+                      inp.descale_v, inp.causal, bm, kl, stream)
+
+    for _ in range(warmup):
+        flush()
+        run()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush()
+        ev[i][0].record(stream)
+        run()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if fa.fa_get_device_status() != 0:
+        raise RuntimeError("device status reports a timed-out wait")
+    return inp, sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+
+
 class _Null:
     def __enter__(self):
         return self
@@ -497,6 +530,22 @@ def run_ours(args):
             "fwd_frac_of_peak": round(xf / (xms["fwd"] * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
             "bwd_frac_of_peak": round(2.5 * xf / (xbwd_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
             "stage_ms": {k2: round(v2, 4) for k2, v2 in xms.items() if k2 not in ("wall_s", "launch")},
+        }
+    if rank == 0 and world == 1 and not args.no_extra:
+        finp, fms = time_fp8_forward(EXTRA_WORKLOAD, max(3, min(args.steps, 10)), 3, torch, fa, flush)
+        fB, fH, fN, fd = finp.q8.shape
+        ff = formula_fwd_flops(fB, fH, fN, fd, finp.causal)
+        fpairs = visited_tile_pairs(fN, finp.causal, finp.kv_len, finp.block_mask, fB, fH)
+        fach = algorithmic_flops(fpairs, fd)["fwd"] / (fms * 1e-3) / 1e12
+        fp8_peak = 2.0 * peaks["bf16_tflops"]
+        line["fp8_forward"] = {
+            "workload": EXTRA_WORKLOAD, "dtype": "e4m3 in, fp32 accumulate, bf16 out",
+            "tflops": round(ff / (fms * 1e-3) / 1e12, 2), "ms": round(fms, 4),
+            "roofline": {"kernel": "fwd_fp8", "bound": "tensor", "achieved": round(fach, 2),
+                         "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(fach / fp8_peak, 4),
+                         "traffic": recorded_traffic("fwd_fp8", EXTRA_WORKLOAD),
+                         "peak_source": f"bf16_tflops burst ({peaks['source']}) x 2, the nominal dense "
+                                        "fp8:bf16 ratio (4.5 : 2.25 PFLOP/s)"},
         }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(args.workload, args.cpu_budget)

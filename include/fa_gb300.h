@@ -77,6 +77,35 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int B, int H, int N, int d, float scale, int causal,
                  const uint8_t* block_mask, const int32_t* kv_len, int dtype, void* stream);
 
+/* Forward pass with 8-bit inputs (OCP FP8 E4M3: 1 sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits, largest finite value 448) and one scale per tensor.  The pages
+ * quote an 8-bit forward only as a throughput figure ("How FlashAttention Bypasses
+ * the GPU Memory Bottleneck to Enable Long-Context AI", factlen.com, the paragraphs
+ * on FlashAttention-3 for Hopper: 8-bit floating point on H100); the arithmetic
+ * below is this library's reading.
+ * The attention inputs are Q = descale_q * q, K = descale_k * k, V = descale_v * v
+ * where q, k, v are the E4M3 codes; the result is the forward of fa_fwd on those
+ * values: O = softmax(scale * Q K^T) V (bf16) and LSE (float32), with the masks,
+ * empty-row rule and LSE definition given above.
+ *  - q, k: E4M3 [B, H, N, d], d fastest.
+ *  - vt: E4M3 V transposed, [B, H, d, ldv]: vt[b,h,c,j] = v[b,h,j,c]; ldv (row stride
+ *    in elements = bytes) must be >= N and a multiple of 16; columns j >= N are not
+ *    read.
+ *  - o: bf16 [B, H, N, d]; lse: float32 [B, H, N].
+ *  - d must be 128 (anything else returns FA_ERR_UNSUPPORTED).  scale and the three
+ *    descale factors must be finite and > 0.
+ * Arithmetic: S = Q K^T and P V are 8-bit tensor-core products accumulated in float
+ * registers of the tensor memory; the softmax is float32.  P (values in (0, 256],
+ * relative to a row max that trails the true one by at most 8 log2 units) is rounded
+ * to E4M3 for the P V product, which moves each probability by at most 2^-4 of
+ * itself (2^-10 absolute below 2^-6); the row sum and LSE use the unrounded values.
+ * O is therefore accurate to a few percent relative (not to bf16 precision); LSE is
+ * as accurate as the score products.
+ * One kernel launch; pointers 16-byte aligned (lse 4-byte); errors as for fa_fwd. */
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, int ldv, void* o, float* lse,
+                     int B, int H, int N, int d, float scale, float descale_q, float descale_k, float descale_v,
+                     int causal, const uint8_t* block_mask, const int32_t* kv_len, void* stream);
+
 /* Bytes of device workspace fa_bwd needs: D = rowsum(dO * O) (float32 [B,H,N])
  * and the float32 dQ accumulator [B,H,N,d], each 256-byte aligned.  Linear in N. */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);

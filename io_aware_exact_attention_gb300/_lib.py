@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libfa_gb300.so")
 
-SOURCES = ["fa_api.cu", "fa_fwd_bf16.cu", "fa_fwd_fp32.cu", "fa_bwd_bf16.cu", "fa_noalloc.cu", "fa_selftest.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_fp32.cu", "fa_bwd_bf16.cu", "fa_noalloc.cu", "fa_selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
 
@@ -82,6 +82,8 @@ def _declare(lib):
     vp, sz, i, f = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, i, vp]
     lib.fa_fwd.restype = i
+    lib.fa_fwd_fp8.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, f, f, f, f, i, vp, vp, vp]
+    lib.fa_fwd_fp8.restype = i
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
     lib.fa_bwd_workspace_size.restype = sz
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, vp, vp, i, vp]

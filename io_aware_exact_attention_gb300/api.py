@@ -65,6 +65,46 @@ def fa_fwd(q, k, v, o, lse, scale, causal=False, block_mask=None, kv_len=None, s
     _check(code, "fa_fwd")
 
 
+_BYTE_TYPES = tuple(t for t in (torch.uint8, getattr(torch, "float8_e4m3fn", None)) if t is not None)
+
+
+def fa_fwd_fp8(q8, k8, vt8, o, lse, scale, descale_q, descale_k, descale_v, causal=False, block_mask=None,
+               kv_len=None, stream=None):
+    """O (bf16), LSE <- attention of E4M3 inputs with per-tensor scales.
+
+    q8, k8: [B,H,N,d] uint8 or float8_e4m3fn; vt8: V transposed, [B,H,d,ldv] with a
+    contiguous last dimension of stride 1 and rows ldv >= N (a multiple of 16) apart;
+    o: bf16 [B,H,N,d]; lse: float32 [B,H,N]."""
+    B, H, N, d = _shape(q8)
+    if q8.dtype not in _BYTE_TYPES or k8.dtype != q8.dtype or vt8.dtype != q8.dtype:
+        raise ValueError("q8, k8, vt8 must be uint8 or float8_e4m3fn tensors of one dtype")
+    if tuple(k8.shape) != (B, H, N, d) or not q8.is_contiguous() or not k8.is_contiguous():
+        raise ValueError("q8 and k8 must be contiguous [B, H, N, d]")
+    if vt8.dim() != 4 or tuple(vt8.shape[:3]) != (B, H, d) or vt8.stride(3) != 1:
+        raise ValueError("vt8 must be [B, H, d, ldv] with unit stride in the last dimension")
+    ldv = int(vt8.stride(2))
+    if vt8.shape[3] < N or vt8.stride(1) != d * ldv or vt8.stride(0) != H * d * ldv:
+        raise ValueError("vt8 rows must hold at least N keys and be packed ldv apart")
+    if o.dtype != torch.bfloat16 or tuple(o.shape) != (B, H, N, d) or not o.is_contiguous():
+        raise ValueError("o must be contiguous bf16 [B, H, N, d]")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
+        raise ValueError("bad lse")
+    code = _lib.load().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), ldv, _ptr(o), _ptr(lse), B, H, N, d, float(scale),
+                                  float(descale_q), float(descale_k), float(descale_v), int(bool(causal)),
+                                  _ptr(block_mask), _ptr(kv_len), _stream(stream))
+    _check(code, "fa_fwd_fp8")
+
+
+def attention_forward_fp8(q8, k8, vt8, scale, descale_q, descale_k, descale_v, causal=False, block_mask=None,
+                          kv_len=None, stream=None):
+    """Allocate O (bf16) and LSE with torch and run fa_fwd_fp8.  Returns (o, lse)."""
+    B, H, N, d = _shape(q8)
+    o = torch.empty((B, H, N, d), device=q8.device, dtype=torch.bfloat16)
+    lse = torch.empty((B, H, N), device=q8.device, dtype=torch.float32)
+    fa_fwd_fp8(q8, k8, vt8, o, lse, scale, descale_q, descale_k, descale_v, causal, block_mask, kv_len, stream)
+    return o, lse
+
+
 def fa_bwd_workspace_size(B, H, N, d) -> int:
     return int(_lib.load().fa_bwd_workspace_size(B, H, N, d))
 

@@ -107,6 +107,21 @@ bool encode_bf16_block32(CUtensorMap* map, const void* base, int BH, int N, int 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 8-bit [B*H, rows, cols] tensor with row stride ld >= cols bytes, boxes of 128 x 128
+// with 128-byte swizzle.  Columns past `cols` and rows past `rows` read as zero.
+bool encode_u8(CUtensorMap* map, const void* base, int BH, int rows, int cols, int ld) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld), static_cast<cuuint64_t>(rows) * ld};
+  const cuuint32_t box[3] = {128, 128, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // float32 [B*H, N, d] tensor (the dQ accumulator), boxes of 32 x 32 with 128-byte
 // swizzle; the backward kernel reduce-adds 32x32 blocks into it.
 bool encode_f32_acc(CUtensorMap* map, const void* base, int BH, int N, int d) {
@@ -131,6 +146,7 @@ fa::AttnArgs make_args(int B, int H, int N, int d, float scale, int causal, cons
   a.n_tiles = (N + fa::kTile - 1) / fa::kTile;
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
+  a.o_scale = 1.f;
   a.causal = causal ? 1 : 0;
   a.block_mask = block_mask;
   a.kv_len = kv_len;
@@ -232,6 +248,35 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     return FA_ERR_CUDA;
   maps.o_ptr = o;
   return launch_status(fa::launch_fwd_bf16(maps, lse, a, s));
+}
+
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, int ldv, void* o, float* lse, int B, int H, int N,
+                     int d, float scale, float descale_q, float descale_k, float descale_v, int causal,
+                     const uint8_t* block_mask, const int32_t* kv_len, void* stream) {
+  bool empty = false;
+  fa_status st = check_shape(B, H, N, d, &empty);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if ((st = check_scale(scale)) != FA_OK || (st = check_scale(descale_q)) != FA_OK ||
+      (st = check_scale(descale_k)) != FA_OK || (st = check_scale(descale_v)) != FA_OK)
+    return st;
+  const float sl2 = scale * descale_q * descale_k * kLog2e;
+  if (!(sl2 > 0.f) || !std::isfinite(sl2)) return FA_ERR_INVALID_ARG;
+  if (empty) return FA_OK;
+  if (ldv < N || ldv % 16 != 0) return FA_ERR_INVALID_ARG;
+  if (!q || !k || !vt || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o) || !aligned4(lse)) return FA_ERR_INVALID_ARG;
+  fa::AttnArgs a = make_args(B, H, N, d, scale, causal, block_mask, kv_len);
+  if (a.status == nullptr) return FA_ERR_CUDA;
+  a.scale_log2 = sl2;
+  a.o_scale = descale_v;
+  fa::FwdMaps maps;
+  const int BH = B * H;
+  if (!encode_u8(&maps.q, q, BH, N, d, d) || !encode_u8(&maps.k, k, BH, N, d, d) ||
+      !encode_u8(&maps.v, vt, BH, d, N, ldv) || !encode_bf16(&maps.o, o, BH, N, d))
+    return FA_ERR_CUDA;
+  maps.o_ptr = o;
+  return launch_status(fa::launch_fwd_fp8(maps, lse, a, static_cast<cudaStream_t>(stream)));
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {

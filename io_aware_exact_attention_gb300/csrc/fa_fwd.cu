@@ -1,4 +1,5 @@
-// Forward pass, bf16 in / fp32 accumulate, on the fifth-generation tensor cores.
+// Forward pass on the fifth-generation tensor cores: bf16 inputs (d = 64 or 128) or
+// FP8 E4M3 inputs (d = 128), fp32 accumulation, bf16 O and fp32 LSE.
 //
 // One CTA owns two adjacent 128-row query tiles Q_a, Q_b of one (batch, head) and
 // streams the key/value tiles K_j, V_j either may see, as in the "FlashAttention
@@ -23,6 +24,15 @@
 // raised only when a tile's max exceeds it by more than kRescaleSlack (in log2
 // units); the result is still exact because O and l always use the same max, and
 // most tiles then skip the O rescale.  S and P never reach HBM.
+//
+// The FP8 variant runs the same kernel with 8-bit tiles.  Q and K arrive as E4M3
+// [B*H, N, 128] (one 128-byte swizzle row per token); V arrives transposed, E4M3
+// [B*H, 128, ldv], so that the P V product reads it K-major (keys contiguous) like
+// the score product reads K.  Both products are kind::f8f6f4 MMAs of K = 32.  The
+// per-tensor scales of Q and K are folded into the score scale and that of V into
+// 1/l.  P is rounded to E4M3 (its values lie in (0, 2^8], see kRescaleSlack) and
+// packed four to a TMEM column; the row sum l is taken over the unrounded values.
+// O (bf16) is staged in a region of its own, the 8-bit Q tiles being half its size.
 #include "fa_internal.h"
 #include "fa_tiles.cuh"
 #include "sm103_ptx.cuh"
@@ -37,17 +47,23 @@ constexpr float kRescaleSlack = 8.0f;  // P values stay below 2^8 before a resca
 // softmax phases overlap each other's MMAs.  NQ = 1 (d = 64): a lighter CTA with
 // 256 TMEM columns and ~81 KB of shared memory, so two CTAs share an SM and one
 // CTA's set-up, loads and epilogue overlap the other's main loop.
-template <int D, int NQ>
+// F8: E4M3 tiles (d = 128, two query tiles).
+template <int D, int NQ, bool F8>
 struct FwdLayout {
+  static_assert(!F8 || (D == 128 && NQ == 2), "the FP8 forward runs d = 128 with two query tiles per CTA");
+  static constexpr int kElem = F8 ? 1 : 2;        // bytes per Q, K or V element
   static constexpr int kThreads = 64 + 128 * NQ;  // producer warp, MMA warp, one softmax warpgroup per tile
   static constexpr int kCtasPerSm = NQ == 1 ? 2 : 1;
-  static constexpr int kStages = NQ == 1 ? 2 : (D == 64 ? 4 : 2);
-  static constexpr int kTileBytes = kTile * D * 2;  // one 128-row tile of Q, K or V (bf16)
-  static constexpr int kSubBytes = kTile * 64 * 2;  // one 64-column swizzle sub-tile
-  static constexpr int kQ = 0;                      // NQ query tiles
+  static constexpr int kStages = F8 ? 4 : (NQ == 1 ? 2 : (D == 64 ? 4 : 2));
+  static constexpr int kTileBytes = kTile * D * kElem;  // one tile of Q, K or V (F8: V^T, d rows x 128 keys)
+  static constexpr int kSubBytes = kTile * 128;         // one swizzle sub-tile: 128 rows of 128 bytes
+  static constexpr int kSubElems = 128 / kElem;         // elements in one sub-tile row
+  static constexpr int kOTileBytes = kTile * D * 2;     // one bf16 O tile
+  static constexpr int kQ = 0;                          // NQ query tiles
   static constexpr int kK = kQ + NQ * kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kEnd = kV + kStages * kTileBytes;
+  static constexpr int kOStage = kV + kStages * kTileBytes;  // F8: O staging; bf16 stages O in the Q tiles
+  static constexpr int kEnd = F8 ? kOStage + NQ * kOTileBytes : kOStage;
   static constexpr int kSmemBytes = kEnd + 1024;  // slack for aligning the base to 1024
   static constexpr uint32_t kTmemCols = NQ == 1 ? 256 : 512;
   // TMEM columns: score/P buffer of tile i at 128*i, output accumulator of tile i after all score buffers
@@ -57,12 +73,12 @@ struct FwdLayout {
   static_assert(kSmemBytes <= (NQ == 1 ? 112 * 1024 : 227 * 1024), "shared memory budget");
 };
 
-template <int D, int NQ>
+template <int S>
 struct FwdBarriers {
   uint64_t q_full;
-  uint64_t k_full[FwdLayout<D, NQ>::kStages];
-  uint64_t v_full[FwdLayout<D, NQ>::kStages];
-  uint64_t kv_empty[FwdLayout<D, NQ>::kStages];
+  uint64_t k_full[S];
+  uint64_t v_full[S];
+  uint64_t kv_empty[S];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
@@ -107,18 +123,16 @@ __device__ __forceinline__ int next_union_tile(const int (&qt)[2], int kt, int k
   return kt;
 }
 
-template <int D, int NQ>
-__global__ void __launch_bounds__(FwdLayout<D, NQ>::kThreads, FwdLayout<D, NQ>::kCtasPerSm)
-    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                    float* __restrict__ lse_out, const AttnArgs a) {
-  using L = FwdLayout<D, NQ>;
+template <int D, int NQ, bool F8>
+__device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                         const CUtensorMap& tm_o, float* __restrict__ lse_out, const AttnArgs& a) {
+  using L = FwdLayout<D, NQ, F8>;
   griddep_launch_dependents();
   griddep_wait();  // every global access of this kernel comes after the previous kernel of the stream
   constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) FwdBarriers<D, NQ> bar;
+  __shared__ __align__(8) FwdBarriers<S> bar;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
 
@@ -172,19 +186,26 @@ __global__ void __launch_bounds__(FwdLayout<D, NQ>::kThreads, FwdLayout<D, NQ>::
       tma_prefetch_desc(&tm_v);
       mbar_arrive_expect_tx(&bar.q_full, (has_b ? 2 : 1) * L::kTileBytes);
       for (int i = 0; i < (has_b ? 2 : 1); ++i)
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(smQ + i * L::kTileBytes + h * L::kSubBytes, &tm_q, &bar.q_full, h * 64, qt[i] * kTile, head);
+        for (int h = 0; h < L::kTileBytes / L::kSubBytes; ++h)
+          tma_load_3d(smQ + i * L::kTileBytes + h * L::kSubBytes, &tm_q, &bar.q_full, h * L::kSubElems,
+                      qt[i] * kTile, head);
       int u = 0;
       bool ok = true;
       for (int kt = next_union_tile(qt, 0, kv_len, a); kt < T; kt = next_union_tile(qt, kt + 1, kv_len, a), ++u) {
         const int s = u % S;
         if (u >= S && !(ok = mbar_wait(&bar.kv_empty[s], ((u / S) - 1) & 1, wc))) break;
         mbar_arrive_expect_tx(&bar.k_full[s], L::kTileBytes);
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(smK + s * L::kTileBytes + h * L::kSubBytes, &tm_k, &bar.k_full[s], h * 64, kt * kTile, head);
+        for (int h = 0; h < L::kTileBytes / L::kSubBytes; ++h)
+          tma_load_3d(smK + s * L::kTileBytes + h * L::kSubBytes, &tm_k, &bar.k_full[s], h * L::kSubElems,
+                      kt * kTile, head);
         mbar_arrive_expect_tx(&bar.v_full[s], L::kTileBytes);
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(smV + s * L::kTileBytes + h * L::kSubBytes, &tm_v, &bar.v_full[s], h * 64, kt * kTile, head);
+        if constexpr (F8) {
+          // V^T tile: d rows of 128 keys
+          tma_load_3d(smV + s * L::kTileBytes, &tm_v, &bar.v_full[s], kt * kTile, 0, head);
+        } else {
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(smV + s * L::kTileBytes + h * L::kSubBytes, &tm_v, &bar.v_full[s], h * 64, kt * kTile, head);
+        }
       }
       if (!ok) {
         // let the loads already issued land before the CTA can exit
@@ -198,8 +219,8 @@ __global__ void __launch_bounds__(FwdLayout<D, NQ>::kThreads, FwdLayout<D, NQ>::
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t idesc_s = F8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_o = F8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D, false, true);
       const uint32_t q0 = smem_u32(smQ), k0 = smem_u32(smK), v0 = smem_u32(smV);
       bool ok = mbar_wait(&bar.q_full, 0, wc);
       int n[2] = {0, 0};  // P V products issued per query tile
@@ -211,10 +232,14 @@ __global__ void __launch_bounds__(FwdLayout<D, NQ>::kThreads, FwdLayout<D, NQ>::
         tc_fence_after();
         const uint32_t qs = q0 + i * L::kTileBytes, ks = k0 + stage * L::kTileBytes;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
+        for (int k = 0; k < D * L::kElem / 32; ++k) {  // 32 bytes of each row per MMA
           const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
-          mma_bf16_ss(tmem + L::col_s(i), sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + off, 16, 1024), idesc_s,
+          if constexpr (F8)
+            mma_f8_ss(tmem + L::col_s(i), sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + off, 16, 1024), idesc_s,
                       k > 0 ? 1u : 0u);
+          else
+            mma_bf16_ss(tmem + L::col_s(i), sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + off, 16, 1024),
+                        idesc_s, k > 0 ? 1u : 0u);
         }
         mma_commit(&bar.s_full[i]);
         (void)kt_s;
@@ -246,10 +271,19 @@ __global__ void __launch_bounds__(FwdLayout<D, NQ>::kThreads, FwdLayout<D, NQ>::
           if (f[i]) {
             if (!(ok = mbar_wait(&bar.p_full[i], n[i] & 1, wc))) break;
             tc_fence_after();
+            if constexpr (F8) {
+              // V^T K-major: 32 keys = 32 bytes per step; P: four keys per TMEM column
 #pragma unroll
-            for (int k = 0; k < kTile / 16; ++k)
-              mma_bf16_ts(tmem + L::col_o(i), tmem + L::col_s(i) + k * 8,
-                          sdesc_sw128(vs + k * 2048, L::kSubBytes, 1024), idesc_o, (n[i] > 0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < kTile / 32; ++k)
+                mma_f8_ts(tmem + L::col_o(i), tmem + L::col_s(i) + k * 8, sdesc_sw128(vs + k * 32, 16, 1024), idesc_o,
+                          (n[i] > 0 || k > 0) ? 1u : 0u);
+            } else {
+              // V N-major: 16 keys = 2048 bytes per step; P: two keys per TMEM column
+#pragma unroll
+              for (int k = 0; k < kTile / 16; ++k)
+                mma_bf16_ts(tmem + L::col_o(i), tmem + L::col_s(i) + k * 8,
+                            sdesc_sw128(vs + k * 2048, L::kSubBytes, 1024), idesc_o, (n[i] > 0 || k > 0) ? 1u : 0u);
+            }
             mma_commit(&bar.o_done[i]);
             ++n[i];
           }
@@ -321,14 +355,22 @@ __global__ void __launch_bounds__(FwdLayout<D, NQ>::kThreads, FwdLayout<D, NQ>::
           s[c + 1] = ex2(s[c + 1]);
         }
         const float tile_sum = row_sum128(s);
-        uint32_t pk[kTile / 2];
-#pragma unroll
-        for (int c = 0; c < kTile; c += 2) pk[c / 2] = pack_bf16x2(s[c], s[c + 1]);
         l_run = l_run * alpha + tile_sum;
         m_run = m_new;
-        // P replaces S in the tile's TMEM buffer (bf16 pairs, columns [0, 64))
-        tmem_st32(t_s, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(t_s + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+        if constexpr (F8) {
+          // P replaces S in the tile's TMEM buffer (E4M3 quads, columns [0, 32))
+          uint32_t pk[kTile / 4];
+#pragma unroll
+          for (int c = 0; c < kTile; c += 4) pk[c / 4] = pack_e4m3x4(s[c], s[c + 1], s[c + 2], s[c + 3]);
+          tmem_st32(t_s, pk);
+        } else {
+          // P replaces S in the tile's TMEM buffer (bf16 pairs, columns [0, 64))
+          uint32_t pk[kTile / 2];
+#pragma unroll
+          for (int c = 0; c < kTile; c += 2) pk[c / 2] = pack_bf16x2(s[c], s[c + 1]);
+          tmem_st32(t_s, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+          tmem_st32(t_s + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+        }
         if (n > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
           // the previous P V must be done before O is rescaled
           ok = mbar_wait(&bar.o_done[wg], (n - 1) & 1, wc);
@@ -354,8 +396,14 @@ __global__ void __launch_bounds__(FwdLayout<D, NQ>::kThreads, FwdLayout<D, NQ>::
         have_o = __all_sync(0xffffffffu, ok);
         tc_fence_after();
       }
-      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-      uint8_t* stage = smQ + wg * L::kTileBytes;
+      if (!F8 && n == 0) {
+        // no score MMA has read this Q tile, so its TMA load may still be landing in
+        // the buffer the zero O is about to be staged in
+        ok = mbar_wait(&bar.q_full, 0, wc);
+        __syncwarp();
+      }
+      const float inv_l = l_run > 0.f ? a.o_scale / l_run : 0.f;
+      uint8_t* stage = F8 ? smem + L::kOStage + wg * L::kOTileBytes : smQ + wg * L::kTileBytes;
       const uint32_t orow = smem_u32(stage);
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -396,6 +444,22 @@ __global__ void __launch_bounds__(FwdLayout<D, NQ>::kThreads, FwdLayout<D, NQ>::
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
+}
+
+template <int D, int NQ>
+__global__ void __launch_bounds__(FwdLayout<D, NQ, false>::kThreads, FwdLayout<D, NQ, false>::kCtasPerSm)
+    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    float* __restrict__ lse_out, const AttnArgs a) {
+  fwd_body<D, NQ, false>(tm_q, tm_k, tm_v, tm_o, lse_out, a);
+}
+
+// tm_v maps V^T (E4M3 [B*H, 128, ldv]).
+__global__ void __launch_bounds__(FwdLayout<128, 2, true>::kThreads, 1)
+    fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   float* __restrict__ lse_out, const AttnArgs a) {
+  fwd_body<128, 2, true>(tm_q, tm_k, tm_v, tm_o, lse_out, a);
 }
 
 // Persistent forward for d = 64: two CTAs per SM, each walking (query tile, head) items
@@ -808,7 +872,7 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
 
 template <int D, int NQ>
 cudaError_t launch_fwd_d(const FwdMaps& maps, float* lse, const AttnArgs& a, cudaStream_t stream) {
-  using L = FwdLayout<D, NQ>;
+  using L = FwdLayout<D, NQ, false>;
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fwd_bf16_kernel<D, NQ>), L::kSmemBytes);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>((a.n_tiles + NQ - 1) / NQ) * a.B * a.H;
@@ -817,6 +881,15 @@ cudaError_t launch_fwd_d(const FwdMaps& maps, float* lse, const AttnArgs& a, cud
 }
 
 }  // namespace
+
+cudaError_t launch_fwd_fp8(const FwdMaps& maps, float* lse, const AttnArgs& a, cudaStream_t stream) {
+  using L = FwdLayout<128, 2, true>;
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fwd_fp8_kernel), L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>((a.n_tiles + 1) / 2) * a.B * a.H;
+  return launch_pdl(fwd_fp8_kernel, static_cast<unsigned>(grid), L::kThreads, L::kSmemBytes, stream, maps.q, maps.k,
+                    maps.v, maps.o, lse, a);
+}
 
 cudaError_t launch_fwd_bf16(const FwdMaps& maps, float* lse, const AttnArgs& a, cudaStream_t stream) {
   if (a.d == 128) return launch_fwd_d<128, 2>(maps, lse, a, stream);

@@ -16,13 +16,17 @@ struct AttnArgs {
   int n_tiles;                // ceil(N / 128)
   float scale;                // softmax scale
   float scale_log2;           // scale * log2(e): scores go straight to the exp2 domain
+                              // (FP8 forward: times the scales of Q and K)
+  float o_scale;              // factor on O / l (FP8 forward: the scale of V; otherwise 1)
   int causal;
   const uint8_t* block_mask;  // [n_tiles, n_tiles] or null
   const int32_t* kv_len;      // [B] or null
   unsigned int* status;       // device status word
 };
 
-// Tensor maps for [B*H, N, d] bf16 tensors, boxes of 64 x 128 with 128-byte swizzle.
+// Tensor maps for [B*H, N, d] bf16 tensors, boxes of 64 x 128 with 128-byte swizzle
+// (FP8 forward: q, k E4M3 [B*H, N, 128] in 128 x 128 boxes, v the E4M3 V^T
+// [B*H, 128, ldv] in 128-key x 128-row boxes, o bf16 as above).
 struct FwdMaps {
   CUtensorMap q, k, v, o;
   void* o_ptr;  // O itself, for rows written with plain stores
@@ -61,6 +65,8 @@ int sm_count();
 cudaError_t ensure_smem_limit(const void* kernel, int bytes);
 
 cudaError_t launch_fwd_bf16(const FwdMaps& maps, float* lse, const AttnArgs& a, cudaStream_t stream);
+
+cudaError_t launch_fwd_fp8(const FwdMaps& maps, float* lse, const AttnArgs& a, cudaStream_t stream);
 
 cudaError_t launch_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse,
                             const AttnArgs& a, cudaStream_t stream);

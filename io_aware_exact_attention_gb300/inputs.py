@@ -62,24 +62,36 @@ def e4m3_bits(x: np.ndarray) -> np.ndarray:
     x = np.asarray(x, dtype=np.float32)
     if np.isnan(x).any():
         raise ValueError("NaN has no place in an E4M3 input")
-    a = np.abs(x).astype(np.float64)
+    a = np.abs(x)
     _, e2 = np.frexp(a)                       # a = f * 2^e2 with f in [0.5, 1)
     e = np.maximum(e2 - 1, -6)                # binade exponent, clamped to the subnormal range
-    q = np.rint(a / np.exp2(e - 3))           # exact division by a power of two; rint is ties-to-even
-    code = np.where(a < 2.0 ** -6, np.rint(a / 2.0 ** -9), (e + 7) * 8 + (q - 8))
+    # a * 2^(3 - e) is exact (a power-of-two scaling); rint rounds ties to even.  In
+    # the subnormal range (e = -6) the same step 2^-9 applies and the code is the
+    # multiple itself, which also carries into the first normal binade.
+    q = np.rint(np.ldexp(a, 3 - e)).astype(np.int32)
+    code = np.where(a < np.float32(2.0 ** -6), q, (e + 7) * 8 + (q - 8))
     if (code > 0x7E).any():
         raise ValueError("value beyond the E4M3 range (|x| rounds above 448)")
     return (code.astype(np.uint8) | np.where(np.signbit(x), 0x80, 0).astype(np.uint8)).astype(np.uint8)
 
 
-def e4m3_bits_to_f32(codes: np.ndarray) -> np.ndarray:
-    """OCP FP8 E4M3 codes -> exactly equal float32 values (0x7F / 0xFF decode to NaN)."""
-    c = np.asarray(codes, dtype=np.uint8).astype(np.int32)
+def _e4m3_values() -> np.ndarray:
+    """Value of each of the 256 E4M3 codes: exponent field 0 gives m * 2^-9, otherwise
+    (8 + m) * 2^(e - 10) = 1.m * 2^(e - 7); 0x7F and 0xFF are NaN."""
+    c = np.arange(256, dtype=np.int32)
     e = (c >> 3) & 0xF
     m = (c & 7).astype(np.float64)
     mag = np.where(e == 0, m * 2.0 ** -9, (8.0 + m) * np.exp2(e - 10.0))
     mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
     return np.where(c & 0x80, -mag, mag).astype(np.float32)
+
+
+_E4M3_VALUES = _e4m3_values()
+
+
+def e4m3_bits_to_f32(codes: np.ndarray) -> np.ndarray:
+    """OCP FP8 E4M3 codes -> exactly equal float32 values (0x7F / 0xFF decode to NaN)."""
+    return _E4M3_VALUES[np.asarray(codes, dtype=np.uint8)]
 
 
 def pow2_scale(x: np.ndarray) -> float:

@@ -95,7 +95,7 @@ def head_rows(q, k, v, dout, scale, *, causal=False, kv_len=None, block_mask=Non
     qh, kh, vh = _f64(q), _f64(k), _f64(v)
     dh = _f64(dout) if dout is not None else None
     n, d = qh.shape
-    kl = n if kv_len is None else int(kv_len)
+    kl = -1 if kv_len is None else min(max(int(kv_len), 0), n)  # -1: no key padding
     rows = np.arange(n, dtype=np.int32) if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
     nr = rows.shape[0]
     o = np.empty((nr, d), np.float64)
@@ -124,7 +124,7 @@ def head_cols(q, k, v, dout, scale, m, l, D, *, causal=False, kv_len=None, block
     lib = _load()
     qh, kh, vh, dh = _f64(q), _f64(k), _f64(v), _f64(dout)
     n, d = qh.shape
-    kl = n if kv_len is None else int(kv_len)
+    kl = -1 if kv_len is None else min(max(int(kv_len), 0), n)  # -1: no key padding
     cols = np.arange(n, dtype=np.int32) if cols is None else np.ascontiguousarray(cols, dtype=np.int32)
     nc = cols.shape[0]
     m = np.ascontiguousarray(m, np.float64)

@@ -239,7 +239,7 @@ static int fill_head(head_t *h, const double *q, const double *k, const double *
   if (block_mask && tile <= 0) return -1;
   h->q = q; h->k = k; h->v = v; h->dout = dout;
   h->N = N; h->d = d; h->scale = scale; h->causal = causal;
-  h->kv_len = (kv_len <= 0 || kv_len > N) ? N : kv_len;
+  h->kv_len = (kv_len < 0 || kv_len > N) ? N : kv_len;
   h->block_mask = block_mask;
   h->tile = tile > 0 ? tile : 1;
   h->n_tiles = (N + h->tile - 1) / h->tile;
@@ -249,7 +249,8 @@ static int fill_head(head_t *h, const double *q, const double *k, const double *
 /* Per-row pass for the query rows rows[0..nrows) of one head.
  * Outputs are indexed by position in `rows`: o[nrows*d], lse, m, l, Dsum [nrows],
  * dq[nrows*d].  dout, m, l, Dsum and dq may be NULL (forward only).
- * kv_len <= 0 means "no key padding".  Returns 0 on success. */
+ * kv_len < 0 means "no key padding"; kv_len = 0 means no key is visible.
+ * Returns 0 on success. */
 int oracle_rows(const double *q, const double *k, const double *v, const double *dout,
                 int N, int d, double scale, int causal, int kv_len,
                 const uint8_t *block_mask, int tile,

@@ -83,6 +83,26 @@ def test_fwd_rejects_bad_arguments_without_launching(lib, args, expect):
 
 
 @pytest.mark.parametrize("args,expect", [
+    (dict(d=64), _lib.FA_ERR_UNSUPPORTED),
+    (dict(ldv=120), _lib.FA_ERR_INVALID_ARG),
+    (dict(ldv=136), _lib.FA_ERR_INVALID_ARG),
+    (dict(dq=0.0), _lib.FA_ERR_INVALID_ARG),
+    (dict(dk=float("inf")), _lib.FA_ERR_INVALID_ARG),
+    (dict(dv=-2.0), _lib.FA_ERR_INVALID_ARG),
+    (dict(scale=1e30, dq=1e30), _lib.FA_ERR_INVALID_ARG),  # the folded score scale overflows
+    (dict(vt=A + 8), _lib.FA_ERR_INVALID_ARG),
+    (dict(k=None), _lib.FA_ERR_INVALID_ARG),
+    (dict(N=0, q=None), _lib.FA_OK),
+])
+def test_fwd_fp8_rejects_bad_arguments_without_launching(lib, args, expect):
+    kw = dict(q=A, k=A, vt=A, ldv=128, B=1, H=1, N=128, d=128, scale=0.125, dq=1.0, dk=1.0, dv=1.0)
+    kw.update(args)
+    rc = lib.fa_fwd_fp8(kw["q"], kw["k"], kw["vt"], kw["ldv"], A, A, kw["B"], kw["H"], kw["N"], kw["d"], kw["scale"],
+                        kw["dq"], kw["dk"], kw["dv"], 0, None, None, None)
+    assert rc == expect
+
+
+@pytest.mark.parametrize("args,expect", [
     (dict(dtype=_lib.FA_FP32), _lib.FA_ERR_UNSUPPORTED),
     (dict(d=96), _lib.FA_ERR_UNSUPPORTED),
     (dict(ws_bytes=100), _lib.FA_ERR_INVALID_ARG),

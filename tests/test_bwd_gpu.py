@@ -41,15 +41,17 @@ def test_ragged_sizes(N, d, causal):
     check(inp, f"N={N} d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_key_padding_zero_grads_for_padded_keys(causal):
-    inp = inputs.make_inputs(4, 2, 384, 64, seed=9, causal=causal, kv_len_range=(1, 384))
-    inp.kv_len[:] = np.array([1, 129, 200, 384], np.int32)
+def test_key_padding_zero_grads_for_padded_keys(causal, d):
+    inp = inputs.make_inputs(5, 2, 384, d, seed=9, causal=causal, kv_len_range=(1, 384))
+    inp.kv_len[:] = np.array([0, 1, 129, 200, 384], np.int32)  # 0: no key, so dQ = dK = dV = 0
     got = run_fwd_bwd(inp)
     ref = oracle_bwd(inp)
     parity.check_grads(got, ref, what="padding")
     for b, n in enumerate(inp.kv_len):
         assert np.all(got["dk"][b, :, n:] == 0) and np.all(got["dv"][b, :, n:] == 0)
+    assert np.all(got["dq"][0] == 0)
 
 
 @pytest.mark.parametrize("d", [64, 128])

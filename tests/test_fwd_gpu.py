@@ -51,12 +51,14 @@ def test_fp32_ragged_sizes(N, d, causal):
     parity.check_forward(o, lse, ro, rl, fp32=True, what=f"fp32 N={N} d={d}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_key_padding_ragged(causal):
-    inp = inputs.make_inputs(4, 2, 384, 64, seed=31, causal=causal, kv_len_range=(1, 384), with_dout=False)
-    inp.kv_len[:] = np.array([1, 129, 200, 384], np.int32)
+def test_key_padding_ragged(causal, d):
+    inp = inputs.make_inputs(5, 2, 384, d, seed=31, causal=causal, kv_len_range=(1, 384), with_dout=False)
+    inp.kv_len[:] = np.array([0, 1, 129, 200, 384], np.int32)  # 0: no key at all
     o, lse = run_fwd(inp)
     ro, rl = oracle_fwd(inp)
+    assert np.all(o[0] == 0) and np.all(np.isneginf(lse[0]))
     parity.check_forward(o, lse, ro, rl, what="key padding")
 
 

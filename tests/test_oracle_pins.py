@@ -124,6 +124,28 @@ def test_uniform_scores_give_mean():
     np.testing.assert_allclose(r["lse"], math.log(13), rtol=1e-14)
 
 
+def test_key_length_zero_and_truncation():
+    """A key length L keeps keys [0, L): the result is attention over K[:L], V[:L]
+    (written out with numpy here), and L = 0 leaves every row without a key: O = 0,
+    LSE = -inf, dQ = 0 (fully masked rows); a length above N means no padding."""
+    rng = np.random.default_rng(15)
+    n, d = 12, 5
+    q, k, v, do = (_rand(rng, n, d) for _ in range(4))
+    for L in (1, 7, n):
+        r = oracle.head_rows(q, k, v, do, 0.6, kv_len=L)
+        s = 0.6 * q @ k[:L].T
+        p = np.exp(s - s.max(1, keepdims=True))
+        np.testing.assert_allclose(r["o"], (p / p.sum(1, keepdims=True)) @ v[:L], rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(r["lse"], s.max(1) + np.log(p.sum(1)), rtol=1e-14)
+    r = oracle.head_rows(q, k, v, do, 0.6, kv_len=0)
+    assert np.all(r["o"] == 0) and np.all(np.isneginf(r["lse"])) and np.all(r["dq"] == 0)
+    full = oracle.head_rows(q, k, v, do, 0.6)
+    np.testing.assert_array_equal(oracle.head_rows(q, k, v, do, 0.6, kv_len=n + 5)["o"], full["o"])
+    out = oracle.attention_backward(q[None, None], k[None, None], v[None, None], do[None, None], 0.6,
+                                    kv_len=np.array([0], np.int32))
+    assert np.all(out["o"] == 0) and np.all(out["dk"] == 0) and np.all(out["dv"] == 0)
+
+
 def test_permutation_equivariance():
     rng = np.random.default_rng(6)
     n, d = 30, 8
