@@ -52,7 +52,10 @@ template <int D, int NQ, bool F8>
 struct FwdLayout {
   static_assert(!F8 || (D == 128 && NQ == 2), "the FP8 forward runs d = 128 with two query tiles per CTA");
   static constexpr int kElem = F8 ? 1 : 2;        // bytes per Q, K or V element
-  static constexpr int kThreads = 64 + 128 * NQ;  // producer warp, MMA warp, one softmax warpgroup per tile
+  // warp 0 producer, warp 1 MMA issuer of tile a, warps 2.. one softmax warpgroup per
+  // tile, then (NQ = 2) the MMA issuer of tile b
+  static constexpr int kIssuerB = NQ == 2 ? 2 + 4 * NQ : -1;
+  static constexpr int kThreads = 64 + 128 * NQ + (NQ == 2 ? 32 : 0);
   static constexpr int kCtasPerSm = NQ == 1 ? 2 : 1;
   static constexpr int kStages = F8 ? 4 : (NQ == 1 ? 2 : (D == 64 ? 4 : 2));
   static constexpr int kTileBytes = kTile * D * kElem;  // one tile of Q, K or V (F8: V^T, d rows x 128 keys)
@@ -78,11 +81,13 @@ struct FwdBarriers {
   uint64_t q_full;
   uint64_t k_full[S];
   uint64_t v_full[S];
-  uint64_t kv_empty[S];
+  uint64_t k_empty[S];  // both score products have read the K tile of the stage
+  uint64_t v_empty[S];  // both P V products have read the V tile of the stage
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
-  uint64_t drain;
+  uint64_t drain[2];  // one per MMA issuer
+  uint64_t tok[2];    // tok[i]: issuer i has issued its batch (the other issuer's turn)
 };
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
@@ -159,14 +164,16 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
     for (int s = 0; s < S; ++s) {
       mbar_init(&bar.k_full[s], 1);
       mbar_init(&bar.v_full[s], 1);
-      mbar_init(&bar.kv_empty[s], 1);
+      mbar_init(&bar.k_empty[s], has_b ? 2 : 1);  // one commit per MMA issuer
+      mbar_init(&bar.v_empty[s], has_b ? 2 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.s_full[i], 1);
       mbar_init(&bar.p_full[i], 128);
       mbar_init(&bar.o_done[i], 1);
+      mbar_init(&bar.drain[i], 1);
+      mbar_init(&bar.tok[i], 1);
     }
-    mbar_init(&bar.drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -180,57 +187,96 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&bar.q_full, (has_b ? 2 : 1) * L::kTileBytes);
-      for (int i = 0; i < (has_b ? 2 : 1); ++i)
-        for (int h = 0; h < L::kTileBytes / L::kSubBytes; ++h)
-          tma_load_3d(smQ + i * L::kTileBytes + h * L::kSubBytes, &tm_q, &bar.q_full, h * L::kSubElems,
-                      qt[i] * kTile, head);
+    // lane 0: both query tiles, then the K tiles; lane 1: the V tiles.  K and V stages
+    // are released separately (a K tile is done once both score products have read
+    // it, a V tile once both P V products have), so K runs ahead of V.
+    if (lane < 2) {
+      const bool is_k = lane == 0;
+      if (is_k) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        mbar_arrive_expect_tx(&bar.q_full, (has_b ? 2 : 1) * L::kTileBytes);
+        for (int i = 0; i < (has_b ? 2 : 1); ++i)
+          for (int h = 0; h < L::kTileBytes / L::kSubBytes; ++h)
+            tma_load_3d(smQ + i * L::kTileBytes + h * L::kSubBytes, &tm_q, &bar.q_full, h * L::kSubElems,
+                        qt[i] * kTile, head);
+      } else {
+        tma_prefetch_desc(&tm_v);
+      }
+      uint64_t* full = is_k ? bar.k_full : bar.v_full;
+      uint64_t* empty = is_k ? bar.k_empty : bar.v_empty;
       int u = 0;
       bool ok = true;
       for (int kt = next_union_tile(qt, 0, kv_len, a); kt < T; kt = next_union_tile(qt, kt + 1, kv_len, a), ++u) {
         const int s = u % S;
-        if (u >= S && !(ok = mbar_wait(&bar.kv_empty[s], ((u / S) - 1) & 1, wc))) break;
-        mbar_arrive_expect_tx(&bar.k_full[s], L::kTileBytes);
-        for (int h = 0; h < L::kTileBytes / L::kSubBytes; ++h)
-          tma_load_3d(smK + s * L::kTileBytes + h * L::kSubBytes, &tm_k, &bar.k_full[s], h * L::kSubElems,
-                      kt * kTile, head);
-        mbar_arrive_expect_tx(&bar.v_full[s], L::kTileBytes);
-        if constexpr (F8) {
+        if (u >= S && !(ok = mbar_wait(&empty[s], ((u / S) - 1) & 1, wc))) break;
+        mbar_arrive_expect_tx(&full[s], L::kTileBytes);
+        if (is_k) {
+          for (int h = 0; h < L::kTileBytes / L::kSubBytes; ++h)
+            tma_load_3d(smK + s * L::kTileBytes + h * L::kSubBytes, &tm_k, &full[s], h * L::kSubElems, kt * kTile,
+                        head);
+        } else if constexpr (F8) {
           // V^T tile: d rows of 128 keys
-          tma_load_3d(smV + s * L::kTileBytes, &tm_v, &bar.v_full[s], kt * kTile, 0, head);
+          tma_load_3d(smV + s * L::kTileBytes, &tm_v, &full[s], kt * kTile, 0, head);
         } else {
           for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(smV + s * L::kTileBytes + h * L::kSubBytes, &tm_v, &bar.v_full[s], h * 64, kt * kTile, head);
+            tma_load_3d(smV + s * L::kTileBytes + h * L::kSubBytes, &tm_v, &full[s], h * 64, kt * kTile, head);
         }
       }
       if (!ok) {
         // let the loads already issued land before the CTA can exit
-        mbar_drain(&bar.q_full, 0, 100000000ull);
-        for (int j = (u > S ? u - S : 0); j < u; ++j) {
-          mbar_drain(&bar.k_full[j % S], (j / S) & 1, 100000000ull);
-          mbar_drain(&bar.v_full[j % S], (j / S) & 1, 100000000ull);
-        }
+        if (is_k) mbar_drain(&bar.q_full, 0, 100000000ull);
+        for (int j = (u > S ? u - S : 0); j < u; ++j) mbar_drain(&full[j % S], (j / S) & 1, 100000000ull);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+  } else if (warp == 1 || warp == L::kIssuerB) {
+    // ------------------------------------------------------------ MMA issuers
+    // One issuing thread per query tile: warp 1 for tile a, warp kIssuerB for tile b.
+    // An MMA holds its issuing thread about as long as the tensor pipe takes to run it,
+    // so with a single issuer its waits and bookkeeping leave the pipe idle.  Here the
+    // two issuers take turns: a batch (tile i's P V, then its next scores) is issued only
+    // after the other tile's batch, signalled through tok[] as soon as its last MMA is
+    // issued; each thread's waits and commits then overlap the other's MMAs, and the
+    // alternation keeps one softmax running while the other tile's products execute.
+    // The two tiles' accumulators and score buffers are disjoint; a K or V stage is
+    // released once both issuers have committed it (k_empty and v_empty count one
+    // arrival per issuer, one commit per key tile of the union list whether the tile
+    // used it or not).  Each issuer runs one batch per key tile of the union list plus
+    // the first scores, used or empty, so the token phases of the two threads stay in
+    // step.
+    const int i = warp == 1 ? 0 : 1;
+    if (lane == 0 && (i == 0 || has_b)) {
       constexpr uint32_t idesc_s = F8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_o = F8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D, false, true);
-      const uint32_t q0 = smem_u32(smQ), k0 = smem_u32(smK), v0 = smem_u32(smV);
+      const uint32_t qs = smem_u32(smQ) + i * L::kTileBytes, k0 = smem_u32(smK), v0 = smem_u32(smV);
+      // Without a block mask the key tiles are [0, end_union) and tile i sees [0, end_i),
+      // which spares the issuer the per-tile visibility tests.
+      const bool dense = a.block_mask == nullptr;
+      const int kvt = (kv_len + kTile - 1) / kTile;
+      const int end_i = min(kvt, a.causal ? qt[i] + 1 : T);
+      const int end_union = has_b ? min(kvt, a.causal ? qt[1] + 1 : T) : min(kvt, a.causal ? qt[0] + 1 : T);
+      auto union_from = [&](int kt) { return dense ? (kt < end_union ? kt : T) : next_union_tile(qt, kt, kv_len, a); };
+      auto sees = [&](int kt) {
+        return dense ? kt < end_i : tile_pair_visible(qt[i], kt, kv_len, a.causal, a.block_mask, T);
+      };
       bool ok = mbar_wait(&bar.q_full, 0, wc);
-      int n[2] = {0, 0};  // P V products issued per query tile
-      int u = 0;          // position in the union list of key tiles
-      // S_i for key tile kt into tile i's TMEM buffer.  That buffer still holds P_i of the
-      // last P V, which this thread issued earlier: MMAs from one thread execute in issue
-      // order, so the new scores overwrite P only after that P V has read it.
-      auto issue_scores = [&](int i, int kt_s, int stage) -> bool {
+      int n = 0;  // P V products issued for this tile
+      int u = 0;  // position in the union list of key tiles
+      // batch j of tile a follows batch j-1 of tile b; batch j of tile b follows batch j of a
+      auto take_turn = [&](int j) -> bool {
+        if (!has_b) return true;
+        if (i == 0) return j == 0 || mbar_wait(&bar.tok[1], (j - 1) & 1, wc);
+        return mbar_wait(&bar.tok[0], j & 1, wc);
+      };
+      auto pass_turn = [&]() {
+        if (has_b) mbar_arrive(&bar.tok[i]);
+      };
+      // S_i for the key tile in `stage` into tile i's TMEM buffer.  That buffer still holds
+      // P_i of the last P V, which this thread issued earlier: MMAs from one thread execute
+      // in issue order, so the new scores overwrite P only after that P V has read it.
+      auto issue_scores = [&](int stage) {
         tc_fence_after();
-        const uint32_t qs = q0 + i * L::kTileBytes, ks = k0 + stage * L::kTileBytes;
+        const uint32_t ks = k0 + stage * L::kTileBytes;
 #pragma unroll
         for (int k = 0; k < D * L::kElem / 32; ++k) {  // 32 bytes of each row per MMA
           const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
@@ -242,67 +288,61 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
                         idesc_s, k > 0 ? 1u : 0u);
         }
         mma_commit(&bar.s_full[i]);
-        (void)kt_s;
-        return true;
       };
-      int kt = next_union_tile(qt, 0, kv_len, a);
+      int kt = union_from(0);
       if (ok && kt < T) {
-        ok = mbar_wait(&bar.k_full[0], 0, wc);
-        for (int i = 0; ok && i < 2; ++i)
-          if (i == 0 || has_b)
-            if (tile_pair_visible(qt[i], kt, kv_len, a.causal, a.block_mask, T)) ok = issue_scores(i, kt, 0);
+        const bool f0 = sees(kt);
+        if (f0) ok = mbar_wait(&bar.k_full[0], 0, wc);
+        if (ok) ok = take_turn(0);
+        if (ok) {
+          if (f0) issue_scores(0);
+          pass_turn();
+          mma_commit(&bar.k_empty[0]);
+        }
       }
-      // Per key tile: P_i V for each tile i, and right after it tile i's scores for the
-      // next key tile, so each softmax warpgroup gets its next scores without waiting
-      // for the other tile.
+      // Per key tile of the union list: P_i V, then S_i for the next key tile, so the
+      // softmax warpgroup gets its next scores as early as possible.  Every V stage is
+      // waited for and every stage committed, used or not: the V wait keeps this thread
+      // from committing a stage ahead of the other issuer's use of its previous contents.
       while (ok && kt < T) {
         const int s = u % S;
-        const int kt_next = next_union_tile(qt, kt + 1, kv_len, a);
-        bool f[2], fn[2];
-        f[0] = tile_pair_visible(qt[0], kt, kv_len, a.causal, a.block_mask, T);
-        f[1] = has_b && tile_pair_visible(qt[1], kt, kv_len, a.causal, a.block_mask, T);
-        fn[0] = kt_next < T && tile_pair_visible(qt[0], kt_next, kv_len, a.causal, a.block_mask, T);
-        fn[1] = kt_next < T && has_b && tile_pair_visible(qt[1], kt_next, kv_len, a.causal, a.block_mask, T);
+        const int kt_next = union_from(kt + 1);
+        const bool f = sees(kt), fn = kt_next < T && sees(kt_next);
         if (!(ok = mbar_wait(&bar.v_full[s], (u / S) & 1, wc))) break;
-        const uint32_t vs = v0 + s * L::kTileBytes;
-        bool next_k_ready = false;
+        if (f && !(ok = mbar_wait(&bar.p_full[i], n & 1, wc))) break;
+        if (!(ok = take_turn(u + 1))) break;
+        if (f) {
+          tc_fence_after();
+          const uint32_t vs = v0 + s * L::kTileBytes;
+          if constexpr (F8) {
+            // V^T K-major: 32 keys = 32 bytes per step; P: four keys per TMEM column
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          if (f[i]) {
-            if (!(ok = mbar_wait(&bar.p_full[i], n[i] & 1, wc))) break;
-            tc_fence_after();
-            if constexpr (F8) {
-              // V^T K-major: 32 keys = 32 bytes per step; P: four keys per TMEM column
+            for (int k = 0; k < kTile / 32; ++k)
+              mma_f8_ts(tmem + L::col_o(i), tmem + L::col_s(i) + k * 8, sdesc_sw128(vs + k * 32, 16, 1024), idesc_o,
+                        (n > 0 || k > 0) ? 1u : 0u);
+          } else {
+            // V N-major: 16 keys = 2048 bytes per step; P: two keys per TMEM column
 #pragma unroll
-              for (int k = 0; k < kTile / 32; ++k)
-                mma_f8_ts(tmem + L::col_o(i), tmem + L::col_s(i) + k * 8, sdesc_sw128(vs + k * 32, 16, 1024), idesc_o,
-                          (n[i] > 0 || k > 0) ? 1u : 0u);
-            } else {
-              // V N-major: 16 keys = 2048 bytes per step; P: two keys per TMEM column
-#pragma unroll
-              for (int k = 0; k < kTile / 16; ++k)
-                mma_bf16_ts(tmem + L::col_o(i), tmem + L::col_s(i) + k * 8,
-                            sdesc_sw128(vs + k * 2048, L::kSubBytes, 1024), idesc_o, (n[i] > 0 || k > 0) ? 1u : 0u);
-            }
-            mma_commit(&bar.o_done[i]);
-            ++n[i];
+            for (int k = 0; k < kTile / 16; ++k)
+              mma_bf16_ts(tmem + L::col_o(i), tmem + L::col_s(i) + k * 8,
+                          sdesc_sw128(vs + k * 2048, L::kSubBytes, 1024), idesc_o, (n > 0 || k > 0) ? 1u : 0u);
           }
-          if (fn[i]) {
-            if (!next_k_ready) {
-              if (!(ok = mbar_wait(&bar.k_full[(u + 1) % S], ((u + 1) / S) & 1, wc))) break;
-              next_k_ready = true;
-            }
-            if (!(ok = issue_scores(i, kt_next, (u + 1) % S))) break;
-          }
+          mma_commit(&bar.o_done[i]);
+          ++n;
         }
-        if (!ok) break;
-        mma_commit(&bar.kv_empty[s]);
+        mma_commit(&bar.v_empty[s]);
+        if (fn) {
+          if (!(ok = mbar_wait(&bar.k_full[(u + 1) % S], ((u + 1) / S) & 1, wc))) break;
+          issue_scores((u + 1) % S);
+        }
+        pass_turn();
+        if (kt_next < T) mma_commit(&bar.k_empty[(u + 1) % S]);
         kt = kt_next;
         ++u;
       }
       if (!ok) {
-        mma_commit(&bar.drain);
-        mbar_drain(&bar.drain, 0, 100000000ull);
+        mma_commit(&bar.drain[i]);
+        mbar_drain(&bar.drain[i], 0, 100000000ull);
       }
     }
   } else {
@@ -455,7 +495,7 @@ __global__ void __launch_bounds__(FwdLayout<D, NQ, false>::kThreads, FwdLayout<D
 }
 
 // tm_v maps V^T (E4M3 [B*H, 128, ldv]).
-__global__ void __launch_bounds__(FwdLayout<128, 2, true>::kThreads, 1)
+__global__ void __launch_bounds__(FwdLayout<128, 2, true>::kThreads, FwdLayout<128, 2, true>::kCtasPerSm)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                    float* __restrict__ lse_out, const AttnArgs a) {
