@@ -287,7 +287,6 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
             mma_bf16_ss(tmem + L::col_s(i), sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + off, 16, 1024),
                         idesc_s, k > 0 ? 1u : 0u);
         }
-        mma_commit(&bar.s_full[i]);
       };
       int kt = union_from(0);
       if (ok && kt < T) {
@@ -295,7 +294,10 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
         if (f0) ok = mbar_wait(&bar.k_full[0], 0, wc);
         if (ok) ok = take_turn(0);
         if (ok) {
-          if (f0) issue_scores(0);
+          if (f0) {
+            issue_scores(0);
+            mma_commit(&bar.s_full[i]);
+          }
           pass_turn();
           mma_commit(&bar.k_empty[0]);
         }
@@ -308,8 +310,10 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
         const int s = u % S;
         const int kt_next = union_from(kt + 1);
         const bool f = sees(kt), fn = kt_next < T && sees(kt_next);
+        // all waits before the turn: inside it only MMAs and the score commit are issued
         if (!(ok = mbar_wait(&bar.v_full[s], (u / S) & 1, wc))) break;
         if (f && !(ok = mbar_wait(&bar.p_full[i], n & 1, wc))) break;
+        if (fn && !(ok = mbar_wait(&bar.k_full[(u + 1) % S], ((u + 1) / S) & 1, wc))) break;
         if (!(ok = take_turn(u + 1))) break;
         if (f) {
           tc_fence_after();
@@ -327,15 +331,19 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
               mma_bf16_ts(tmem + L::col_o(i), tmem + L::col_s(i) + k * 8,
                           sdesc_sw128(vs + k * 2048, L::kSubBytes, 1024), idesc_o, (n > 0 || k > 0) ? 1u : 0u);
           }
+        }
+        if (fn) {
+          issue_scores((u + 1) % S);
+          mma_commit(&bar.s_full[i]);
+        }
+        pass_turn();
+        // The P V completion (o_done) is signalled after the next scores: the softmax waits
+        // for it only after it has waited for those scores, which complete no earlier.
+        if (f) {
           mma_commit(&bar.o_done[i]);
           ++n;
         }
         mma_commit(&bar.v_empty[s]);
-        if (fn) {
-          if (!(ok = mbar_wait(&bar.k_full[(u + 1) % S], ((u + 1) / S) & 1, wc))) break;
-          issue_scores((u + 1) % S);
-        }
-        pass_turn();
         if (kt_next < T) mma_commit(&bar.k_empty[(u + 1) % S]);
         kt = kt_next;
         ++u;
