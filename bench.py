@@ -345,6 +345,43 @@ def time_fp8_forward(name, steps, warmup, torch, fa, flush):
     return inp, sum(e[0].elapsed_time(e[1]) for e in ev) / steps
 
 
+def time_splitkv(name, steps, warmup, torch, fa, flush):
+    """fa_fwd_splitkv on a query block / key cache workload (automatic split count; both
+    launches of the call inside each event pair; L2 flushed between steps).  Returns
+    (inputs, n_splits, mean ms per call)."""
+    inp = inputs.qk_workload_inputs(name)
+    B, H, Nq, d = inp.q.shape
+    Nk = inp.k.shape[2]
+
+    def dev(n):
+        return torch.from_numpy(inp.device_array(n).view(np.int16)).view(torch.bfloat16).cuda()
+
+    q, k, v = dev("q"), dev("k"), dev("v")
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), device="cuda", dtype=torch.float32)
+    n_splits = fa.fa_fwd_splitkv_pick_splits(B, H, Nq, Nk)
+    ws = torch.empty(fa.fa_fwd_splitkv_workspace_size(B, H, Nq, d, n_splits), device="cuda", dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+
+    def run():
+        fa.fa_fwd_splitkv(q, k, v, o, lse, inp.scale, None, n_splits, ws, stream)
+
+    for _ in range(warmup):
+        flush()
+        run()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush()
+        ev[i][0].record(stream)
+        run()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if fa.fa_get_device_status() != 0:
+        raise RuntimeError("device status reports a timed-out wait")
+    return inp, n_splits, sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+
+
 class _Null:
     def __enter__(self):
         return self
@@ -547,6 +584,23 @@ def run_ours(args):
                          "peak_source": f"bf16_tflops burst ({peaks['source']}) x 2, the nominal dense "
                                         "fp8:bf16 ratio (4.5 : 2.25 PFLOP/s)"},
         }
+    if rank == 0 and world == 1 and not args.no_extra:
+        line["split_kv"] = {}
+        for qk_name in sorted(inputs.QK_WORKLOADS):
+            sin, n_splits, sms = time_splitkv(qk_name, max(3, min(args.steps, 20)), 3, torch, fa, flush)
+            sB, sH, sNq, sd = sin.q.shape
+            sNk = sin.k.shape[2]
+            flops = 4.0 * sB * sH * sNq * sNk * sd
+            nbytes = 2.0 * (2 * sB * sH * sNk * sd + 2 * sB * sH * sNq * sd) + 4.0 * sB * sH * sNq  # K, V, Q, O, LSE
+            gbs = nbytes / (sms * 1e-3) / 1e9
+            line["split_kv"][qk_name] = {
+                "config": {"B": sB, "H": sH, "Nq": sNq, "Nk": sNk, "d": sd, "n_splits": n_splits},
+                "ms": round(sms, 4), "tflops": round(flops / (sms * 1e-3) / 1e12, 2),
+                "roofline": {"kernel": "fwd_splitkv + combine (one call)", "bound": "hbm", "achieved": round(gbs, 1),
+                             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                             "traffic": None,
+                             "algorithmic_bytes": "Q, K, V read once, O (bf16) and LSE written"},
+            }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(args.workload, args.cpu_budget)
     if rank == 0:

@@ -106,6 +106,38 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, int ldv, void
                      int B, int H, int N, int d, float scale, float descale_q, float descale_k, float descale_v,
                      int causal, const uint8_t* block_mask, const int32_t* kv_len, void* stream);
 
+/* Split-KV forward for short query blocks against long keys (decode and chunked
+ * prefill).  Not on the pages: their kernels split work over query tiles, which
+ * leaves most SMs idle when B*H*ceil(Nq/128) is small; this entry point also splits
+ * the keys of each query tile into n_splits chunks processed in parallel and merges
+ * the partial results by their log-sum-exp, which gives the same softmax over all keys
+ * (the online-softmax rescaling of "The Trick: Online Softmax" applied across chunks
+ * instead of across tiles).
+ *  - q: bf16 [B, H, Nq, d]; k, v: bf16 [B, H, Nk, d] (Nq and Nk independent, either
+ *    may exceed the other); o: bf16 [B, H, Nq, d]; lse: float32 [B, H, Nq].
+ *  - No causal or block mask: every query row sees keys j < kv_len[b] (all Nk keys if
+ *    kv_len is NULL; lengths clamped to [0, Nk]).  Rows that see no key get O = 0,
+ *    LSE = -inf; so does every row when Nk = 0 (k and v may then be NULL).
+ *  - d must be 128 (anything else returns FA_ERR_UNSUPPORTED).
+ *  - n_splits: key chunks per 128-row query tile, 1..1024; each chunk of
+ *    ceil(ceil(Nk/128) / n_splits) key tiles yields two partial results (its even and
+ *    odd key tiles, processed side by side by one CTA).  fa_fwd_splitkv_pick_splits
+ *    suggests a value giving about one CTA per SM.
+ *  - workspace: caller-owned device memory of at least
+ *    fa_fwd_splitkv_workspace_size(B, H, Nq, d, n_splits) bytes, 16-byte aligned:
+ *    float32 partial O [2*n_splits, B*H, Nq, d] and partial LSE [2*n_splits, B*H, Nq].
+ * Two kernel launches (partials, then the combine).  Errors as for fa_fwd. */
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int Nq, int Nk, int d, float scale, const int32_t* kv_len,
+                         int n_splits, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes fa_fwd_splitkv needs (0 for an empty problem or n_splits < 1). */
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int d, int n_splits);
+
+/* A key-chunk count for fa_fwd_splitkv: enough CTAs for about one per SM of the
+ * current device, at least two key tiles per chunk, at most 1024; 1 for empty shapes. */
+int fa_fwd_splitkv_pick_splits(int B, int H, int Nq, int Nk);
+
 /* Bytes of device workspace fa_bwd needs: D = rowsum(dO * O) (float32 [B,H,N])
  * and the float32 dQ accumulator [B,H,N,d], each 256-byte aligned.  Linear in N. */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);

@@ -84,6 +84,12 @@ def _declare(lib):
     lib.fa_fwd.restype = i
     lib.fa_fwd_fp8.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, f, f, f, f, i, vp, vp, vp]
     lib.fa_fwd_fp8.restype = i
+    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, i, vp, sz, vp]
+    lib.fa_fwd_splitkv.restype = i
+    lib.fa_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i]
+    lib.fa_fwd_splitkv_workspace_size.restype = sz
+    lib.fa_fwd_splitkv_pick_splits.argtypes = [i, i, i, i]
+    lib.fa_fwd_splitkv_pick_splits.restype = i
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
     lib.fa_bwd_workspace_size.restype = sz
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, vp, vp, i, vp]

@@ -105,6 +105,49 @@ def attention_forward_fp8(q8, k8, vt8, scale, descale_q, descale_k, descale_v, c
     return o, lse
 
 
+def fa_fwd_splitkv_workspace_size(B, H, Nq, d, n_splits) -> int:
+    return int(_lib.load().fa_fwd_splitkv_workspace_size(B, H, Nq, d, n_splits))
+
+
+def fa_fwd_splitkv_pick_splits(B, H, Nq, Nk) -> int:
+    return int(_lib.load().fa_fwd_splitkv_pick_splits(B, H, Nq, Nk))
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, scale, kv_len=None, n_splits=None, workspace=None, stream=None):
+    """O, LSE <- attention of Q [B,H,Nq,d] over K, V [B,H,Nk,d] (bf16, no causal mask),
+    the keys of each query tile split into n_splits chunks whose partial results are
+    merged by their log-sum-exp.  workspace: a uint8 CUDA tensor of at least
+    fa_fwd_splitkv_workspace_size(...) bytes (allocated here when None)."""
+    B, H, Nq, d = _shape(q)
+    Nk = int(k.shape[2])
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise ValueError("split-KV forward takes bf16 tensors")
+    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
+        raise ValueError("k and v must be [B, H, Nk, d]")
+    _same(q, o)
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq):
+        raise ValueError("bad lse")
+    if n_splits is None:
+        n_splits = fa_fwd_splitkv_pick_splits(B, H, Nq, Nk)
+    if workspace is None:
+        nbytes = fa_fwd_splitkv_workspace_size(B, H, Nq, d, n_splits)
+        workspace = torch.empty(max(nbytes, 16), device=q.device, dtype=torch.uint8)
+    code = _lib.load().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, float(scale),
+                                      _ptr(kv_len), int(n_splits), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(code, "fa_fwd_splitkv")
+
+
+def attention_forward_splitkv(q, k, v, scale, kv_len=None, n_splits=None, stream=None):
+    """Allocate O and LSE (and the workspace) with torch and run fa_fwd_splitkv."""
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], device=q.device, dtype=torch.float32)
+    fa_fwd_splitkv(q, k, v, o, lse, scale, kv_len, n_splits, None, stream)
+    return o, lse
+
+
 def fa_bwd_workspace_size(B, H, N, d) -> int:
     return int(_lib.load().fa_bwd_workspace_size(B, H, N, d))
 

@@ -20,6 +20,7 @@ namespace {
 __device__ unsigned int g_fa_status = 0u;
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 1024;  // split-KV: key chunks per query tile
 constexpr float kLog2e = 1.44269504088896340736f;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u; }
@@ -147,6 +148,12 @@ fa::AttnArgs make_args(int B, int H, int N, int d, float scale, int causal, cons
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
   a.o_scale = 1.f;
+  a.nk = N;
+  a.nk_tiles = a.n_tiles;
+  a.n_chunks = 0;
+  a.chunk_tiles = 0;
+  a.part_o = nullptr;
+  a.part_lse = nullptr;
   a.causal = causal ? 1 : 0;
   a.block_mask = block_mask;
   a.kv_len = kv_len;
@@ -277,6 +284,60 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, int ldv, void
     return FA_ERR_CUDA;
   maps.o_ptr = o;
   return launch_status(fa::launch_fwd_fp8(maps, lse, a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int d, int n_splits) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || d <= 0 || n_splits <= 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * Nq * 2 * static_cast<size_t>(n_splits);
+  return round256(rows * d * sizeof(float)) + round256(rows * sizeof(float));
+}
+
+int fa_fwd_splitkv_pick_splits(int B, int H, int Nq, int Nk) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0) return 1;
+  const long long ctas_per_split = static_cast<long long>(B) * H * ((Nq + fa::kTile - 1) / fa::kTile);
+  const long long key_tiles = (Nk + fa::kTile - 1) / fa::kTile;
+  long long n = (fa::sm_count() + ctas_per_split - 1) / ctas_per_split;  // about one CTA per SM
+  const long long most = (key_tiles + 1) / 2;                              // two key tiles per CTA at least
+  if (n > most) n = most;
+  if (n > kMaxSplits) n = kMaxSplits;
+  return static_cast<int>(n < 1 ? 1 : n);
+}
+
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                         int d, float scale, const int32_t* kv_len, int n_splits, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  bool empty = false;
+  fa_status st = check_shape(B, H, Nq, d, &empty);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (Nk < 0 || n_splits < 1 || n_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (empty) return FA_OK;
+  bool empty_k = false;
+  if (Nk > 0 && (st = check_shape(B, H, Nk, d, &empty_k)) != FA_OK) return st;
+  const long long grid = static_cast<long long>(B) * H * ((Nq + fa::kTile - 1) / fa::kTile) * n_splits;
+  if (grid > INT_MAX) return FA_ERR_INVALID_ARG;
+  if (!q || !o || !lse || !workspace || (Nk > 0 && (!k || !v))) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || !aligned4(lse) || !aligned16(workspace) ||
+      (Nk > 0 && (!aligned16(k) || !aligned16(v))))
+    return FA_ERR_INVALID_ARG;
+  if (workspace_bytes < fa_fwd_splitkv_workspace_size(B, H, Nq, d, n_splits)) return FA_ERR_INVALID_ARG;
+  fa::AttnArgs a = make_args(B, H, Nq, d, scale, 0, nullptr, kv_len);
+  if (a.status == nullptr) return FA_ERR_CUDA;
+  a.nk = Nk;
+  a.nk_tiles = (Nk + fa::kTile - 1) / fa::kTile;
+  a.n_chunks = n_splits;
+  a.chunk_tiles = a.nk_tiles > 0 ? (a.nk_tiles + n_splits - 1) / n_splits : 0;
+  const size_t parts_rows = static_cast<size_t>(B) * H * Nq * 2 * static_cast<size_t>(n_splits);
+  a.part_o = static_cast<float*>(workspace);
+  a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(parts_rows * d * sizeof(float)));
+  fa::FwdMaps maps;
+  const int BH = B * H;
+  if (!encode_bf16(&maps.q, q, BH, Nq, d)) return FA_ERR_CUDA;
+  if (Nk > 0 && (!encode_bf16(&maps.k, k, BH, Nk, d) || !encode_bf16(&maps.v, v, BH, Nk, d))) return FA_ERR_CUDA;
+  maps.o = maps.q;  // not used by the partial pass
+  maps.o_ptr = o;
+  return launch_status(fa::launch_fwd_splitkv(maps, o, lse, a, static_cast<cudaStream_t>(stream)));
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {

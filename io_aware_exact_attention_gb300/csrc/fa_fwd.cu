@@ -128,7 +128,10 @@ __device__ __forceinline__ int next_union_tile(const int (&qt)[2], int kt, int k
   return kt;
 }
 
-template <int D, int NQ, bool F8>
+// SPLIT: split-KV partial pass (bf16, d = 128): the CTA's two query-tile slots hold the
+// same query tile and see the even / odd key tiles of one key chunk; each slot writes a
+// normalised float32 O and its LSE as one partial result instead of O.
+template <int D, int NQ, bool F8, bool SPLIT = false>
 __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                          const CUtensorMap& tm_o, float* __restrict__ lse_out, const AttnArgs& a) {
   using L = FwdLayout<D, NQ, F8>;
@@ -143,15 +146,53 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int T = a.n_tiles;
-  const int n_groups = (T + NQ - 1) / NQ;
-  const int head = blockIdx.x / n_groups;  // b * H + h
-  const int gr = static_cast<int>(blockIdx.x % n_groups);
-  const int group = a.causal ? (n_groups - 1 - gr) : gr;  // causal: heaviest groups first
-  const int qt[2] = {NQ * group, NQ == 2 ? 2 * group + 1 : T};  // qt[1] >= T: no second tile
+  const int T = a.n_tiles;                  // query tiles
+  const int TK = SPLIT ? a.nk_tiles : T;    // key tiles
+  int head, qt[2], chunk = 0;
+  if constexpr (SPLIT) {
+    const int per_head = T * a.n_chunks;
+    head = blockIdx.x / per_head;
+    const int rem = static_cast<int>(blockIdx.x % per_head);
+    qt[0] = qt[1] = rem / a.n_chunks;
+    chunk = rem % a.n_chunks;
+  } else {
+    const int n_groups = (T + NQ - 1) / NQ;
+    head = blockIdx.x / n_groups;  // b * H + h
+    const int gr = static_cast<int>(blockIdx.x % n_groups);
+    const int group = a.causal ? (n_groups - 1 - gr) : gr;  // causal: heaviest groups first
+    qt[0] = NQ * group;
+    qt[1] = NQ == 2 ? 2 * group + 1 : T;  // qt[1] >= T: no second tile
+  }
   const bool has_b = qt[1] < T;
   const int b = head / a.H;
-  const int kv_len = clamp_kv_len(a.kv_len, b, a.N);
+  const int kv_len = clamp_kv_len(a.kv_len, b, SPLIT ? a.nk : a.N);
+  const int kvt = (kv_len + kTile - 1) / kTile;
+  // SPLIT: key tiles [k_lo, k_hi) of this CTA; slot i sees those at even (i = 0) or odd
+  // (i = 1) positions from k_lo.
+  const int k_lo = SPLIT ? chunk * a.chunk_tiles : 0;
+  const int k_hi = SPLIT ? min(k_lo + a.chunk_tiles, kvt) : TK;
+  // does slot i see key tile kt; first key tile >= kt that slot i sees / either slot sees
+  auto pair_vis = [&](int i, int kt) -> bool {
+    if constexpr (SPLIT) return kt >= k_lo && kt < k_hi && ((kt - k_lo) & 1) == i;
+    else return tile_pair_visible(qt[i], kt, kv_len, a.causal, a.block_mask, T);
+  };
+  auto next_vis = [&](int i, int kt) -> int {
+    if constexpr (SPLIT) {
+      kt = max(kt, k_lo);
+      kt += ((kt - k_lo) & 1) != i;
+      return kt < k_hi ? kt : TK;
+    } else {
+      return next_key_tile(qt[i], kt, kv_len, a.causal, a.block_mask, T);
+    }
+  };
+  auto next_union = [&](int kt) -> int {
+    if constexpr (SPLIT) {
+      kt = max(kt, k_lo);
+      return kt < k_hi ? kt : TK;
+    } else {
+      return next_union_tile(qt, kt, kv_len, a);
+    }
+  };
   const WaitCtx wc{&abort_flag, a.status};
 
   uint8_t* smQ = smem + L::kQ;
@@ -207,7 +248,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
       uint64_t* empty = is_k ? bar.k_empty : bar.v_empty;
       int u = 0;
       bool ok = true;
-      for (int kt = next_union_tile(qt, 0, kv_len, a); kt < T; kt = next_union_tile(qt, kt + 1, kv_len, a), ++u) {
+      for (int kt = next_union(0); kt < TK; kt = next_union(kt + 1), ++u) {
         const int s = u % S;
         if (u >= S && !(ok = mbar_wait(&empty[s], ((u / S) - 1) & 1, wc))) break;
         mbar_arrive_expect_tx(&full[s], L::kTileBytes);
@@ -251,14 +292,11 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
       const uint32_t qs = smem_u32(smQ) + i * L::kTileBytes, k0 = smem_u32(smK), v0 = smem_u32(smV);
       // Without a block mask the key tiles are [0, end_union) and tile i sees [0, end_i),
       // which spares the issuer the per-tile visibility tests.
-      const bool dense = a.block_mask == nullptr;
-      const int kvt = (kv_len + kTile - 1) / kTile;
+      const bool dense = !SPLIT && a.block_mask == nullptr;
       const int end_i = min(kvt, a.causal ? qt[i] + 1 : T);
       const int end_union = has_b ? min(kvt, a.causal ? qt[1] + 1 : T) : min(kvt, a.causal ? qt[0] + 1 : T);
-      auto union_from = [&](int kt) { return dense ? (kt < end_union ? kt : T) : next_union_tile(qt, kt, kv_len, a); };
-      auto sees = [&](int kt) {
-        return dense ? kt < end_i : tile_pair_visible(qt[i], kt, kv_len, a.causal, a.block_mask, T);
-      };
+      auto union_from = [&](int kt) { return dense ? (kt < end_union ? kt : TK) : next_union(kt); };
+      auto sees = [&](int kt) { return dense ? kt < end_i : pair_vis(i, kt); };
       bool ok = mbar_wait(&bar.q_full, 0, wc);
       int n = 0;  // P V products issued for this tile
       int u = 0;  // position in the union list of key tiles
@@ -289,7 +327,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
         }
       };
       int kt = union_from(0);
-      if (ok && kt < T) {
+      if (ok && kt < TK) {
         const bool f0 = sees(kt);
         if (f0) ok = mbar_wait(&bar.k_full[0], 0, wc);
         if (ok) ok = take_turn(0);
@@ -306,10 +344,10 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
       // softmax warpgroup gets its next scores as early as possible.  Every V stage is
       // waited for and every stage committed, used or not: the V wait keeps this thread
       // from committing a stage ahead of the other issuer's use of its previous contents.
-      while (ok && kt < T) {
+      while (ok && kt < TK) {
         const int s = u % S;
         const int kt_next = union_from(kt + 1);
-        const bool f = sees(kt), fn = kt_next < T && sees(kt_next);
+        const bool f = sees(kt), fn = kt_next < TK && sees(kt_next);
         // all waits before the turn: inside it only MMAs and the score commit are issued
         if (!(ok = mbar_wait(&bar.v_full[s], (u / S) & 1, wc))) break;
         if (f && !(ok = mbar_wait(&bar.p_full[i], n & 1, wc))) break;
@@ -344,7 +382,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
           ++n;
         }
         mma_commit(&bar.v_empty[s]);
-        if (kt_next < T) mma_commit(&bar.k_empty[(u + 1) % S]);
+        if (kt_next < TK) mma_commit(&bar.k_empty[(u + 1) % S]);
         kt = kt_next;
         ++u;
       }
@@ -369,8 +407,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
       float l_run = 0.f;        // running sum of exp2(s - m_run)
       bool ok = true;
       int n = 0;
-      for (int kt = next_key_tile(my_qt, 0, kv_len, a.causal, a.block_mask, T); kt < T;
-           kt = next_key_tile(my_qt, kt + 1, kv_len, a.causal, a.block_mask, T), ++n) {
+      for (int kt = next_vis(wg, 0); kt < TK; kt = next_vis(wg, kt + 1), ++n) {
         ok = mbar_wait(&bar.s_full[wg], n & 1, wc);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
@@ -444,13 +481,39 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
         have_o = __all_sync(0xffffffffu, ok);
         tc_fence_after();
       }
+      const float inv_l = l_run > 0.f ? a.o_scale / l_run : 0.f;
+      if constexpr (SPLIT) {
+        // partial result (slot wg of key chunk `chunk`): normalised O in float32 and LSE,
+        // written straight from registers, 512 bytes per row; the TMEM loads are
+        // warp-wide, only the stores are limited to rows below N
+        const bool row_ok = q_row < a.N;
+        const size_t part = static_cast<size_t>(2 * chunk + wg) * (static_cast<size_t>(a.B) * a.H) + head;
+        float4* dst = reinterpret_cast<float4*>(a.part_o + (part * a.N + (row_ok ? q_row : 0)) * D);
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t t[32];
+          if (have_o) {
+            tmem_ld32(t_o + c0, t);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) t[i] = 0u;
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[c0 / 4 + q] = make_float4(__uint_as_float(t[4 * q]) * inv_l, __uint_as_float(t[4 * q + 1]) * inv_l,
+                                            __uint_as_float(t[4 * q + 2]) * inv_l, __uint_as_float(t[4 * q + 3]) * inv_l);
+          }
+        }
+        if (row_ok)
+          a.part_lse[part * a.N + q_row] = (n > 0 && l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : neg_inf();
+      } else {
       if (!F8 && n == 0) {
         // no score MMA has read this Q tile, so its TMA load may still be landing in
         // the buffer the zero O is about to be staged in
         ok = mbar_wait(&bar.q_full, 0, wc);
         __syncwarp();
       }
-      const float inv_l = l_run > 0.f ? a.o_scale / l_run : 0.f;
       uint8_t* stage = F8 ? smem + L::kOStage + wg * L::kOTileBytes : smQ + wg * L::kTileBytes;
       const uint32_t orow = smem_u32(stage);
 #pragma unroll
@@ -483,6 +546,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
         const float lse = (n > 0 && l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : neg_inf();
         lse_out[static_cast<size_t>(head) * a.N + q_row] = lse;
       }
+      }  // !SPLIT
     }
   }
 
@@ -500,6 +564,55 @@ __global__ void __launch_bounds__(FwdLayout<D, NQ, false>::kThreads, FwdLayout<D
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     float* __restrict__ lse_out, const AttnArgs a) {
   fwd_body<D, NQ, false>(tm_q, tm_k, tm_v, tm_o, lse_out, a);
+}
+
+// Split-KV partial pass: tm_q maps Q ([B*H, N, 128]), tm_k and tm_v K and V
+// ([B*H, nk, 128]); tm_o and lse_out are not used.
+__global__ void __launch_bounds__(FwdLayout<128, 2, false>::kThreads, FwdLayout<128, 2, false>::kCtasPerSm)
+    fwd_splitkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                       float* __restrict__ lse_out, const AttnArgs a) {
+  fwd_body<128, 2, false, true>(tm_q, tm_k, tm_v, tm_o, lse_out, a);
+}
+
+// Combine of the split-KV partials, one warp per query row (d = 128, four columns per
+// lane): LSE = M + ln sum_p exp(LSE_p - M) with M = max_p LSE_p, and
+// O = sum_p exp(LSE_p - LSE) O_p, which is the softmax over all keys because each O_p is
+// normalised by its own sum exp(LSE_p).  A row without keys (every LSE_p = -inf, or no
+// partials) gets O = 0 and LSE = -inf.
+__global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __restrict__ part_o,
+                                                              const float* __restrict__ part_lse,
+                                                              uint16_t* __restrict__ o, float* __restrict__ lse,
+                                                              long long rows, int parts) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float m = neg_inf();
+  for (int p = lane; p < parts; p += 32) m = fmaxf(m, part_lse[p * rows + row]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float total = neg_inf();
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (m != neg_inf()) {
+    float sum = 0.f;
+    for (int p = lane; p < parts; p += 32) sum += expf(part_lse[p * rows + row] - m);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    total = m + logf(sum);
+    for (int p = 0; p < parts; ++p) {
+      const float w = expf(part_lse[p * rows + row] - total);
+      if (w == 0.f) continue;  // the same for every lane of the warp
+      const float4 x = reinterpret_cast<const float4*>(part_o + (p * rows + row) * 128)[lane];
+      acc.x += w * x.x;
+      acc.y += w * x.y;
+      acc.z += w * x.z;
+      acc.w += w * x.w;
+    }
+  }
+  reinterpret_cast<uint2*>(o + row * 128)[lane] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  if (lane == 0) lse[row] = total;
 }
 
 // tm_v maps V^T (E4M3 [B*H, 128, ldv]).
@@ -929,6 +1042,24 @@ cudaError_t launch_fwd_d(const FwdMaps& maps, float* lse, const AttnArgs& a, cud
 }
 
 }  // namespace
+
+cudaError_t launch_fwd_splitkv(const FwdMaps& maps, void* o, float* lse, const AttnArgs& a, cudaStream_t stream) {
+  using L = FwdLayout<128, 2, false>;
+  const long long rows = static_cast<long long>(a.B) * a.H * a.N;
+  if (a.n_chunks > 0 && a.nk > 0) {
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fwd_splitkv_kernel), L::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const long long grid = static_cast<long long>(a.n_tiles) * a.n_chunks * a.B * a.H;
+    e = launch_pdl(fwd_splitkv_kernel, static_cast<unsigned>(grid), L::kThreads, L::kSmemBytes, stream, maps.q, maps.k,
+                   maps.v, maps.o, lse, a);
+    if (e != cudaSuccess) return e;
+  }
+  const int parts = (a.n_chunks > 0 && a.nk > 0) ? 2 * a.n_chunks : 0;
+  const long long blocks = (rows * 32 + 255) / 256;
+  return launch_pdl(splitkv_combine_kernel, static_cast<unsigned>(blocks), 256, 0, stream,
+                    static_cast<const float*>(a.part_o), static_cast<const float*>(a.part_lse),
+                    static_cast<uint16_t*>(o), lse, rows, parts);
+}
 
 cudaError_t launch_fwd_fp8(const FwdMaps& maps, float* lse, const AttnArgs& a, cudaStream_t stream) {
   using L = FwdLayout<128, 2, true>;

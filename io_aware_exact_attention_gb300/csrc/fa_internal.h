@@ -22,6 +22,14 @@ struct AttnArgs {
   const uint8_t* block_mask;  // [n_tiles, n_tiles] or null
   const int32_t* kv_len;      // [B] or null
   unsigned int* status;       // device status word
+  // Split-KV forward only (otherwise nk = N, nk_tiles = n_tiles, n_chunks = 0): N and
+  // n_tiles count query rows and tiles, nk and nk_tiles key rows and tiles.  Each CTA
+  // takes key tiles [c * chunk_tiles, (c + 1) * chunk_tiles) of one query tile and writes
+  // two partial results (its even and its odd key tiles) for the combine kernel.
+  int nk, nk_tiles;
+  int n_chunks, chunk_tiles;
+  float* part_o;              // [2 * n_chunks, B*H, N, d] float32, O of each partial (normalised)
+  float* part_lse;            // [2 * n_chunks, B*H, N] float32, LSE of each partial (-inf: no key)
 };
 
 // Tensor maps for [B*H, N, d] bf16 tensors, boxes of 64 x 128 with 128-byte swizzle
@@ -67,6 +75,9 @@ cudaError_t ensure_smem_limit(const void* kernel, int bytes);
 cudaError_t launch_fwd_bf16(const FwdMaps& maps, float* lse, const AttnArgs& a, cudaStream_t stream);
 
 cudaError_t launch_fwd_fp8(const FwdMaps& maps, float* lse, const AttnArgs& a, cudaStream_t stream);
+
+// Split-KV forward (d = 128, bf16): the partial pass then the combine kernel.
+cudaError_t launch_fwd_splitkv(const FwdMaps& maps, void* o, float* lse, const AttnArgs& a, cudaStream_t stream);
 
 cudaError_t launch_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse,
                             const AttnArgs& a, cudaStream_t stream);

@@ -257,6 +257,53 @@ def workload_fp8_inputs(name: str, *, seed: int | None = None, **override) -> Fp
     return make_fp8_inputs(seed=WORKLOAD_SEEDS[name] if seed is None else seed, **spec)
 
 
+@dataclass
+class QKInputs:
+    """Host copies of a query block against a separate key/value sequence (decode and
+    chunked prefill): q float32 [B, H, Nq, d], k, v float32 [B, H, Nk, d], all holding
+    bf16-exact values; no causal mask."""
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    scale: float
+    kv_len: np.ndarray | None
+    seed: int
+
+    def device_array(self, name: str) -> np.ndarray:
+        return bf16_bits(getattr(self, name))
+
+
+def make_qk_inputs(B: int, H: int, Nq: int, Nk: int, d: int, *, seed: int, scale: float | None = None,
+                   kv_len_range: tuple[int, int] | None = None) -> QKInputs:
+    """Q ~ N(0,1) [B,H,Nq,d] and K, V ~ N(0,1) [B,H,Nk,d] rounded to bf16, one stream per
+    tensor as in make_inputs; key lengths uniform on kv_len_range when given."""
+    rq, rk, rv, _rdo, rlen, _rmask, _ = _streams(seed, 7)
+    q = round_bf16(rq.standard_normal((B, H, Nq, d), dtype=np.float32))
+    k = round_bf16(rk.standard_normal((B, H, Nk, d), dtype=np.float32))
+    v = round_bf16(rv.standard_normal((B, H, Nk, d), dtype=np.float32))
+    kv_len = None
+    if kv_len_range is not None:
+        lo, hi = kv_len_range
+        kv_len = rlen.integers(lo, hi + 1, size=B, dtype=np.int64).astype(np.int32)
+    return QKInputs(q=q, k=k, v=v, scale=(1.0 / math.sqrt(d)) if scale is None else float(scale), kv_len=kv_len,
+                    seed=seed)
+
+
+# Split-KV workloads: a 128-row query block (chunked prefill, speculative decoding) and
+# single-token decode against a 32k-token key/value cache, d = 128.
+QK_WORKLOADS = {
+    "prefill_chunk_32k": dict(B=4, H=32, Nq=128, Nk=32768, d=128),
+    "decode_32k": dict(B=8, H=32, Nq=1, Nk=32768, d=128),
+}
+QK_WORKLOAD_SEEDS = {"prefill_chunk_32k": 1006, "decode_32k": 1007}
+
+
+def qk_workload_inputs(name: str, **override) -> QKInputs:
+    spec = dict(QK_WORKLOADS[name])
+    spec.update(override)
+    return make_qk_inputs(seed=QK_WORKLOAD_SEEDS[name], **spec)
+
+
 def workload_inputs(name: str, *, seed: int | None = None, **override) -> AttentionInputs:
     """Inputs of a named workload (optionally with B/H/N overridden for small cases)."""
     spec = dict(WORKLOADS[name])
