@@ -106,7 +106,7 @@ def load_peaks():
 
 def kernel_source_digest(kernel):
     import hashlib
-    src = {"bwd_main": "fa_bwd_bf16.cu", "fwd": "fa_fwd.cu", "fwd_fp8": "fa_fwd.cu"}.get(kernel)
+    src = {"bwd_main": "fa_bwd_bf16.cu", "fwd": "fa_fwd.cu", "fwd_fp8": "fa_fwd.cu", "fwd_splitkv": "fa_fwd.cu"}.get(kernel)
     if src is None:
         return None
     h = hashlib.sha256()
@@ -598,7 +598,7 @@ def run_ours(args):
                 "ms": round(sms, 4), "tflops": round(flops / (sms * 1e-3) / 1e12, 2),
                 "roofline": {"kernel": "fwd_splitkv + combine (one call)", "bound": "hbm", "achieved": round(gbs, 1),
                              "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                             "traffic": None,
+                             "traffic": recorded_traffic("fwd_splitkv", qk_name),
                              "algorithmic_bytes": "Q, K, V read once, O (bf16) and LSE written"},
             }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

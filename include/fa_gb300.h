@@ -134,8 +134,9 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
 /* Workspace bytes fa_fwd_splitkv needs (0 for an empty problem or n_splits < 1). */
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int d, int n_splits);
 
-/* A key-chunk count for fa_fwd_splitkv: enough CTAs for about one per SM of the
- * current device, at least two key tiles per chunk, at most 1024; 1 for empty shapes. */
+/* A key-chunk count for fa_fwd_splitkv on the current device: about six CTAs per SM
+ * for query blocks of at most 16 rows (decode), about half a CTA per SM otherwise; at
+ * least two key tiles per chunk, at most 1024; 1 for empty shapes. */
 int fa_fwd_splitkv_pick_splits(int B, int H, int Nq, int Nk);
 
 /* Bytes of device workspace fa_bwd needs: D = rowsum(dO * O) (float32 [B,H,N])

@@ -296,8 +296,15 @@ int fa_fwd_splitkv_pick_splits(int B, int H, int Nq, int Nk) {
   if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0) return 1;
   const long long ctas_per_split = static_cast<long long>(B) * H * ((Nq + fa::kTile - 1) / fa::kTile);
   const long long key_tiles = (Nk + fa::kTile - 1) / fa::kTile;
-  long long n = (fa::sm_count() + ctas_per_split - 1) / ctas_per_split;  // about one CTA per SM
-  const long long most = (key_tiles + 1) / 2;                              // two key tiles per CTA at least
+  // The pass streams K and V from HBM.  With a few query rows the partial results are a
+  // few hundred bytes, and six CTAs per SM keep more loads in flight (measured on the
+  // 1-row, 32k-key decode shape: 1.05x over one CTA per SM).  A full 128-row block's
+  // partials (2 x 64 KB per CTA) cost more than they hide, so half an SM's worth of
+  // CTAs per split is enough there (128 rows x 32k keys: one split was fastest).
+  const long long sms = fa::sm_count();
+  const long long want = Nq <= 16 ? 6 * sms : sms / 2;
+  long long n = (want + ctas_per_split - 1) / ctas_per_split;
+  const long long most = (key_tiles + 1) / 2;  // two key tiles per CTA at least
   if (n > most) n = most;
   if (n > kMaxSplits) n = kMaxSplits;
   return static_cast<int>(n < 1 ? 1 : n);
