@@ -103,6 +103,41 @@ def test_fwd_fp8_rejects_bad_arguments_without_launching(lib, args, expect):
 
 
 @pytest.mark.parametrize("args,expect", [
+    (dict(d=64), _lib.FA_ERR_UNSUPPORTED),
+    (dict(n_splits=0), _lib.FA_ERR_INVALID_ARG),
+    (dict(n_splits=1025), _lib.FA_ERR_INVALID_ARG),
+    (dict(Nk=-1), _lib.FA_ERR_INVALID_ARG),
+    (dict(ws_bytes=1000), _lib.FA_ERR_INVALID_ARG),
+    (dict(ws=A + 4), _lib.FA_ERR_INVALID_ARG),
+    (dict(k=None), _lib.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), _lib.FA_ERR_INVALID_ARG),
+    (dict(Nq=0, q=None), _lib.FA_OK),
+])
+def test_fwd_splitkv_rejects_bad_arguments_without_launching(lib, args, expect):
+    kw = dict(q=A, k=A, v=A, B=1, H=2, Nq=1, Nk=4096, d=128, scale=0.125, n_splits=4, ws=A)
+    kw.update(args)
+    ws_bytes = kw.get("ws_bytes", lib.fa_fwd_splitkv_workspace_size(1, 2, max(kw["Nq"], 1), 128, 4))
+    rc = lib.fa_fwd_splitkv(kw["q"], kw["k"], kw["v"], A, A, kw["B"], kw["H"], kw["Nq"], kw["Nk"], kw["d"],
+                            kw["scale"], None, kw["n_splits"], kw["ws"], ws_bytes, None)
+    assert rc == expect
+
+
+def test_splitkv_workspace_and_split_choice(lib):
+    # two partials per chunk: float32 O rows and LSE, each 256-byte aligned
+    for (B, H, Nq, n) in [(1, 1, 1, 1), (4, 32, 128, 2), (8, 32, 1, 4)]:
+        rows = B * H * Nq * 2 * n
+        assert lib.fa_fwd_splitkv_workspace_size(B, H, Nq, 128, n) == \
+            ((rows * 128 * 4 + 255) // 256) * 256 + ((rows * 4 + 255) // 256) * 256
+    assert lib.fa_fwd_splitkv_workspace_size(1, 1, 1, 128, 0) == 0
+    for (B, H, Nq, Nk) in [(8, 32, 1, 32768), (4, 32, 128, 32768), (1, 1, 128, 32768), (1, 1, 1, 300),
+                           (64, 64, 2048, 256), (1, 1, 1, 1)]:
+        n = lib.fa_fwd_splitkv_pick_splits(B, H, Nq, Nk)
+        key_tiles = (Nk + 127) // 128
+        assert 1 <= n <= max(1, (key_tiles + 1) // 2) and n <= 1024
+    assert lib.fa_fwd_splitkv_pick_splits(0, 1, 1, 1) == 1
+
+
+@pytest.mark.parametrize("args,expect", [
     (dict(dtype=_lib.FA_FP32), _lib.FA_ERR_UNSUPPORTED),
     (dict(d=96), _lib.FA_ERR_UNSUPPORTED),
     (dict(ws_bytes=100), _lib.FA_ERR_INVALID_ARG),
