@@ -92,6 +92,41 @@ struct FwdBarriers {
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
+// Waits of the MMA issuers, which have nothing else to do meanwhile: try_wait with a
+// suspend-time hint, so the thread sleeps until the phase completes (or the hint runs
+// out) instead of re-issuing the test, leaving the issue slots of its sub-partition
+// to the softmax warps that share it.  Bounded like mbar_wait.
+constexpr uint32_t kIssuerSleepNs = 2000;
+
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kIssuerSleepNs)
+      : "memory");
+  return ok != 0u;
+}
+
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long start = globaltimer();
+  uint32_t tries = 0;
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if ((++tries & 7u) == 0u) {
+      if (*w.abort_flag) return false;
+      if (globaltimer() - start > kWaitLimitNs) {
+        *w.abort_flag = 1;
+        if (w.status) atomicCAS(w.status, 0u, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // Maximum of a 128-value row: eight independent 3-input max chains of eight steps,
 // then a three-level tree (a two-chain loop is a 32-step latency chain).
 __device__ __forceinline__ float row_max128(const float (&v)[kTile]) {
@@ -303,8 +338,8 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
       // batch j of tile a follows batch j-1 of tile b; batch j of tile b follows batch j of a
       auto take_turn = [&](int j) -> bool {
         if (!has_b) return true;
-        if (i == 0) return j == 0 || mbar_wait(&bar.tok[1], (j - 1) & 1, wc);
-        return mbar_wait(&bar.tok[0], j & 1, wc);
+        if (i == 0) return j == 0 || mbar_wait_sleep(&bar.tok[1], (j - 1) & 1, wc);
+        return mbar_wait_sleep(&bar.tok[0], j & 1, wc);
       };
       auto pass_turn = [&]() {
         if (has_b) mbar_arrive(&bar.tok[i]);
@@ -349,9 +384,9 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
         const int kt_next = union_from(kt + 1);
         const bool f = sees(kt), fn = kt_next < TK && sees(kt_next);
         // all waits before the turn: inside it only MMAs and the score commit are issued
-        if (!(ok = mbar_wait(&bar.v_full[s], (u / S) & 1, wc))) break;
-        if (f && !(ok = mbar_wait(&bar.p_full[i], n & 1, wc))) break;
-        if (fn && !(ok = mbar_wait(&bar.k_full[(u + 1) % S], ((u + 1) / S) & 1, wc))) break;
+        if (!(ok = mbar_wait_sleep(&bar.v_full[s], (u / S) & 1, wc))) break;
+        if (f && !(ok = mbar_wait_sleep(&bar.p_full[i], n & 1, wc))) break;
+        if (fn && !(ok = mbar_wait_sleep(&bar.k_full[(u + 1) % S], ((u + 1) / S) & 1, wc))) break;
         if (!(ok = take_turn(u + 1))) break;
         if (f) {
           tc_fence_after();
