@@ -95,7 +95,8 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 // Waits of the MMA issuers, which have nothing else to do meanwhile: try_wait with a
 // suspend-time hint, so the thread sleeps until the phase completes (or the hint runs
 // out) instead of re-issuing the test, leaving the issue slots of its sub-partition
-// to the softmax warps that share it.  Bounded like mbar_wait.
+// to the softmax warps that share it.  Bounded like mbar_wait.  (In the backward
+// kernels the same change made the issuers react later and cost ~3%, so they poll.)
 constexpr uint32_t kIssuerSleepNs = 2000;
 
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
@@ -882,16 +883,16 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
       int u = 0;  // pairs so far (= S and P V products, = K/V ring uses)
       FwdCursor cur = pfwd_cursor_from(0, 0, c, G, n_items, a);
       if (cur.j >= 0) {
-        ok = mbar_wait(&bar.q_full[0], 0, wc) && mbar_wait(&bar.k_full[0], 0, wc);
+        ok = mbar_wait_sleep(&bar.q_full[0], 0, wc) && mbar_wait_sleep(&bar.k_full[0], 0, wc);
         if (ok) issue_scores(cur, 0);
       }
       // The next scores go out as soon as the softmax warps have read these out of TMEM:
       // before this pair's P V inside an item, after it across items (the next item's Q
       // may wait for this item's epilogue, which waits for this P V).
       auto next_scores = [&](const FwdCursor& cur, const FwdCursor& nxt) -> bool {
-        if (nxt.j != cur.j && !mbar_wait(&bar.q_full[nxt.k & 1], (nxt.k >> 1) & 1, wc)) return false;
-        if (!mbar_wait(&bar.k_full[(u + 1) % S], ((u + 1) / S) & 1, wc)) return false;
-        if (!mbar_wait(&bar.s_free, u & 1, wc)) return false;
+        if (nxt.j != cur.j && !mbar_wait_sleep(&bar.q_full[nxt.k & 1], (nxt.k >> 1) & 1, wc)) return false;
+        if (!mbar_wait_sleep(&bar.k_full[(u + 1) % S], ((u + 1) / S) & 1, wc)) return false;
+        if (!mbar_wait_sleep(&bar.s_free, u & 1, wc)) return false;
         issue_scores(nxt, (u + 1) % S);
         return true;
       };
@@ -901,9 +902,9 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
         if (nxt.j == cur.j && !(ok = next_scores(cur, nxt))) break;
         // O (+)= P V; the first product of an item overwrites the accumulator, which the
         // epilogue of the CTA's previous item with a visible key tile must have read out
-        if (!(ok = mbar_wait(&bar.v_full[s], (u / S) & 1, wc))) break;
-        if (!(ok = mbar_wait(&bar.p_full, u & 1, wc))) break;
-        if (cur.first && cur.k >= 1 && !(ok = mbar_wait(&bar.o_free, (cur.k - 1) & 1, wc))) break;
+        if (!(ok = mbar_wait_sleep(&bar.v_full[s], (u / S) & 1, wc))) break;
+        if (!(ok = mbar_wait_sleep(&bar.p_full, u & 1, wc))) break;
+        if (cur.first && cur.k >= 1 && !(ok = mbar_wait_sleep(&bar.o_free, (cur.k - 1) & 1, wc))) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < kTile / 16; ++k)
