@@ -90,6 +90,14 @@ def test_fp8_block_mask_with_empty_rows():
     check_all(inp, o, lse)
 
 
+def test_fp8_causal_block_mask_and_padding():
+    inp = inputs.make_fp8_inputs(2, 2, 900, 128, seed=46, causal=True, kv_len_range=(200, 900),
+                                 block_mask=dict(band=1, global_cols=1, frac=0.3))
+    inp.block_mask[3, :] = 0  # a query tile that sees nothing: its CTA partner still works
+    o, lse = run(inp)
+    check_all(inp, o, lse)
+
+
 def test_fp8_identical_keys_exact_probabilities():
     # every visible key has the same score, so every P' is exactly 1 (exact in E4M3):
     # O_i = the mean of the visible V rows, to bf16 precision
