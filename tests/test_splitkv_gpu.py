@@ -103,3 +103,11 @@ def test_splitkv_workloads_sampled(name):
     heads = [(int(rng.integers(B)), int(rng.integers(H))) for _ in range(3)]
     rows = np.unique(np.concatenate([[0, Nq - 1], rng.integers(0, Nq, 16)]))
     check(inp, o, lse, heads=heads, rows=rows)
+
+
+def test_splitkv_decode_beyond_l2():
+    """Decode of one query row against 16384 keys for B2 H32 (K, V 268 MB, twice the
+    129 MB L2), automatic split count; sampled heads against the oracle."""
+    inp = inputs.make_qk_inputs(2, 32, 1, 16384, 128, seed=12)
+    o, lse = run(inp, None)
+    check(inp, o, lse, heads=[(0, 0), (1, 17), (1, 31)])
