@@ -104,6 +104,14 @@ def load_peaks():
         return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def _code_only(text):
+    """Source text without comments, trailing blanks and blank lines, so that editing a
+    comment does not count as changing a kernel."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_digest(kernel):
     import hashlib
     src = {"bwd_main": "fa_bwd_bf16.cu", "fwd": "fa_fwd.cu", "fwd_fp8": "fa_fwd.cu", "fwd_splitkv": "fa_fwd.cu"}.get(kernel)
@@ -111,7 +119,8 @@ def kernel_source_digest(kernel):
         return None
     h = hashlib.sha256()
     for name in (src, "sm103_ptx.cuh", "fa_tiles.cuh"):
-        h.update(open(os.path.join(ROOT, "io_aware_exact_attention_gb300", "csrc", name), "rb").read())
+        with open(os.path.join(ROOT, "io_aware_exact_attention_gb300", "csrc", name)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -7,12 +7,13 @@
 // (khetwal.com): per key tile it forms the score block, updates the running row
 // max and row sum, rescales the output accumulator and adds P V ("The Trick:
 // Online Softmax").  The GB300 mapping:
-//   warp 0       TMA producer: both query tiles once, then K_j and V_j into a ring
-//                of shared-memory stages (128-byte swizzle), skipping masked tiles;
-//   warp 1       allocates tensor memory and issues tcgen05.mma:
-//                  S_a = Q_a K_j^T, S_b = Q_b K_j^T into two TMEM score buffers,
-//                  O_a += P_a V_j, O_b += P_b V_j with P read from TMEM (the score
-//                  buffer it replaced) and V N-major straight from its TMA tile;
+//   warp 0       TMA producer: lane 0 both query tiles once, then K_j, lane 1 V_j,
+//                each into a ring of shared-memory stages (128-byte swizzle) with
+//                its own release barrier, skipping masked tiles;
+//   warps 1, 10  MMA issuers, one per query tile (warp 1 also allocates tensor
+//                memory), taking turns: tile i's O_i += P_i V_j with P read from
+//                TMEM (the score buffer it replaced) and V N-major straight from
+//                its TMA tile, then S_i = Q_i K_{j+1}^T into that score buffer;
 //   warps 2..5   softmax of tile a, warps 6..9 softmax of tile b: one thread per
 //                query row (one TMEM lane) loads its score row, masks, takes the
 //                max, exponentiates with exp2 (log2 e folded into the scale),

@@ -81,3 +81,12 @@ def test_warmup_floor():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "1"], capture_output=True,
                        text=True, timeout=120)
     assert r.returncode != 0
+
+
+def test_kernel_digest_ignores_comments_only():
+    a = "int f(int x) {  // scale\n  return 2 * x; /* twice */\n}\n"
+    b = "// a new comment\nint f(int x) {\n\n  return 2 * x;\n}\n"
+    c = "int f(int x) {\n  return 3 * x;\n}\n"
+    assert bench._code_only(a) == bench._code_only(b) != bench._code_only(c)
+    assert bench.kernel_source_digest("bwd_main") != bench.kernel_source_digest("fwd")
+    assert bench.kernel_source_digest("no_such_kernel") is None
