@@ -122,7 +122,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, int ldv, void
  *  - n_splits: key chunks per 128-row query tile, 1..1024; each chunk of
  *    ceil(ceil(Nk/128) / n_splits) key tiles yields two partial results (its even and
  *    odd key tiles, processed side by side by one CTA).  fa_fwd_splitkv_pick_splits
- *    suggests a value giving about one CTA per SM.
+ *    suggests a value for the current device.
  *  - workspace: caller-owned device memory of at least
  *    fa_fwd_splitkv_workspace_size(B, H, Nq, d, n_splits) bytes, 16-byte aligned:
  *    float32 partial O [2*n_splits, B*H, Nq, d] and partial LSE [2*n_splits, B*H, Nq].
