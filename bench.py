@@ -94,6 +94,14 @@ def algorithmic_flops(pairs, d):
     return {"fwd": pairs * 4.0 * TILE * TILE * d, "bwd": pairs * 10.0 * TILE * TILE * d}
 
 
+def splitkv_work(B, H, Nq, Nk, d):
+    """Forward FLOPs (4 * Nq * Nk * d per head, no mask) and algorithmic bytes of a
+    split-KV call: K and V read once, Q read, O (bf16) and LSE (fp32) written."""
+    flops = 4.0 * B * H * Nq * Nk * d
+    nbytes = 2.0 * (2 * B * H * Nk * d + 2 * B * H * Nq * d) + 4.0 * B * H * Nq
+    return flops, nbytes
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -599,8 +607,7 @@ def run_ours(args):
             sin, n_splits, sms = time_splitkv(qk_name, max(3, min(args.steps, 20)), 3, torch, fa, flush)
             sB, sH, sNq, sd = sin.q.shape
             sNk = sin.k.shape[2]
-            flops = 4.0 * sB * sH * sNq * sNk * sd
-            nbytes = 2.0 * (2 * sB * sH * sNk * sd + 2 * sB * sH * sNq * sd) + 4.0 * sB * sH * sNq  # K, V, Q, O, LSE
+            flops, nbytes = splitkv_work(sB, sH, sNq, sNk, sd)
             gbs = nbytes / (sms * 1e-3) / 1e9
             line["split_kv"][qk_name] = {
                 "config": {"B": sB, "H": sH, "Nq": sNq, "Nk": sNk, "d": sd, "n_splits": n_splits},

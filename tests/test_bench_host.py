@@ -90,3 +90,12 @@ def test_kernel_digest_ignores_comments_only():
     assert bench._code_only(a) == bench._code_only(b) != bench._code_only(c)
     assert bench.kernel_source_digest("bwd_main") != bench.kernel_source_digest("fwd")
     assert bench.kernel_source_digest("no_such_kernel") is None
+
+
+def test_splitkv_work_counts():
+    # decode: 8 x 32 heads, one query row against 32768 keys, d = 128
+    flops, nbytes = bench.splitkv_work(8, 32, 1, 32768, 128)
+    assert flops == 4 * 256 * 32768 * 128
+    kv = 2 * 256 * 32768 * 128 * 2          # K and V in bf16
+    assert nbytes == kv + 2 * 256 * 128 * 2 + 256 * 4  # + Q and O rows in bf16, LSE in fp32
+    assert abs(kv - 4.295e9) < 1e6           # the 4.30 GB the traffic capture reads
