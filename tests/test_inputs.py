@@ -45,3 +45,20 @@ def test_fp32_workload_not_rounded():
     assert a.dtype == "fp32" and a.q.dtype == np.float32
     assert not np.array_equal(inputs.round_bf16(a.q), a.q)
     assert a.device_array("q") is a.q
+
+
+def test_qk_inputs_shapes_determinism_and_rounding():
+    a = inputs.make_qk_inputs(2, 3, 5, 300, 128, seed=4, kv_len_range=(10, 300))
+    b = inputs.make_qk_inputs(2, 3, 5, 300, 128, seed=4, kv_len_range=(10, 300))
+    assert a.q.shape == (2, 3, 5, 128) and a.k.shape == a.v.shape == (2, 3, 300, 128)
+    for n in ("q", "k", "v"):
+        x = getattr(a, n)
+        np.testing.assert_array_equal(x, getattr(b, n))
+        np.testing.assert_array_equal(inputs.round_bf16(x), x)  # bf16-exact
+        np.testing.assert_array_equal(inputs.bf16_bits_to_f32(a.device_array(n)), x)
+    assert a.kv_len.shape == (2,) and np.all((a.kv_len >= 10) & (a.kv_len <= 300))
+    # Q uses the same stream as make_inputs with that seed
+    sq = inputs.make_inputs(2, 3, 5, 128, seed=4, with_dout=False)
+    np.testing.assert_array_equal(sq.q, a.q)
+    for name, spec in inputs.QK_WORKLOADS.items():
+        assert name in inputs.QK_WORKLOAD_SEEDS and spec["d"] == 128
