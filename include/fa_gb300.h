@@ -163,8 +163,9 @@ fa_status fa_bwd_preprocess(const void* o, const void* dout, void* workspace, si
                             int B, int H, int N, int d, void* stream);
 
 /* Backward stage 2: one CTA per 128-key tile recomputes P for every query tile that
- * sees it and accumulates dK, dV (written as bf16) and dQ (float32 atomics into the
- * workspace accumulator).  Needs stage 1 to have run on the same workspace. */
+ * sees it and accumulates dK, dV (written as bf16) and dQ (added into the workspace's
+ * float32 accumulator by TMA reduce-add, cp.reduce.async.bulk.tensor .add, one 32x32
+ * block at a time).  Needs stage 1 to have run on the same workspace. */
 fa_status fa_bwd_main(const void* q, const void* k, const void* v, const float* lse, const void* dout,
                       void* dk, void* dv, void* workspace, size_t workspace_bytes,
                       int B, int H, int N, int d, float scale, int causal,
@@ -191,9 +192,10 @@ fa_status fa_bwd_postprocess(void* dq, const void* workspace, size_t workspace_b
  *    scratch than FA_BWD_NOALLOC_MAX_BYTES (that is, when
  *    fa_bwd_workspace_size(B,H,N,d) > FA_BWD_NOALLOC_MAX_BYTES; for d = 64 about
  *    258k query rows B*H*N, for d = 128 about 130k);
- *  - the first call on a device looks up the array's device address (with that
- *    device current) and caches it; make that first call before any stream
- *    capture;
+ *  - every call looks up the array's device address on the current device with
+ *    cudaGetSymbolAddress (a host-side query that allocates nothing); the first
+ *    call on a device may also load the library's module there, so make that
+ *    first call before any stream capture;
  *  - every call on a device shares the one array and leaves its contents behind;
  *    the call clears what must start at zero itself, but calls whose work
  *    overlaps on the GPU (different streams, no ordering) race on the array and

@@ -188,6 +188,8 @@ fa_status launch_status(cudaError_t e) {
 }  // namespace
 
 namespace fa {
+int cuda_status(cudaError_t e) { return launch_status(e); }
+
 cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
   struct Entry {
     const void* kernel;

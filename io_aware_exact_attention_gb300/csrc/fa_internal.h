@@ -65,6 +65,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, 
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Records `e` as this host thread's last CUDA error (read by fa_last_cuda_error) and
+// returns the public status for it: FA_OK for cudaSuccess, FA_ERR_CUDA otherwise.
+int cuda_status(cudaError_t e);
+
 // Streaming multiprocessors of the current device (cached after the first call).
 int sm_count();
 

@@ -8,37 +8,20 @@
 // the library itself: a file-scope __device__ array of FA_BWD_NOALLOC_MAX_BYTES,
 // which every GPU that loads the library keeps until the process exits.
 //
-// The array's name in host code is only a host-side handle, not a device address;
-// the device address is looked up with cudaGetSymbolAddress once per device (on
-// that device's first call, with the device current) and then passed to the
-// existing backward kernels like any caller-owned workspace.  Nothing here calls
-// cudaMalloc, cudaFree or any allocating library routine.
+// The array's name in host code is only a host-side handle, not a device address.
+// Every call looks the device address up with cudaGetSymbolAddress on the current
+// device (a host-side query, no allocation) and passes it to the existing backward
+// kernels like any caller-owned workspace.  Looking it up on every call rather than
+// caching it keeps the address right after a device reset reloads the module.
+// Nothing here calls cudaMalloc, cudaFree or any allocating library routine.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "../../include/fa_gb300.h"
+#include "fa_internal.h"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_bwd_scratch[FA_BWD_NOALLOC_MAX_BYTES];
-
-constexpr int kMaxDevices = 64;
-
-// Device address of g_bwd_scratch on the current device, or null on failure.
-void* scratch_address() {
-  static void* addr[kMaxDevices] = {};
-  static std::mutex mu;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr) return nullptr;
-    addr[dev] = p;
-  }
-  return addr[dev];
-}
 
 }  // namespace
 
@@ -55,8 +38,10 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   const size_t need = fa_bwd_workspace_size(B, H, N, d);
   if (need == 0 || need > static_cast<size_t>(FA_BWD_NOALLOC_MAX_BYTES)) return FA_ERR_INVALID_ARG;
-  void* scratch = scratch_address();
-  if (scratch == nullptr) return FA_ERR_CUDA;
+  void* scratch = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&scratch, g_bwd_scratch);
+  if (e != cudaSuccess) return static_cast<fa_status>(fa::cuda_status(e));
+  if (scratch == nullptr) return static_cast<fa_status>(fa::cuda_status(cudaErrorInvalidSymbol));
   // fa_bwd's first stage writes D and zeroes the dQ accumulator in the scratch, so
   // whatever an earlier call left there is overwritten before it is read.
   return fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scratch, static_cast<size_t>(FA_BWD_NOALLOC_MAX_BYTES), B, H, N,

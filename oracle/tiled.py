@@ -1,26 +1,37 @@
-"""The pages' tiled online-softmax algorithm, restated in fp64 numpy.
+"""Blocked softmax attention in fp64 numpy, built from mergeable per-block states.
 
-TEST INFRASTRUCTURE ONLY (see oracle/__init__.py).  It exists so the tests can
-check the method's exactness claim -- the tiled result equals the materialised
-softmax result ("numerically identical", khetwal.com, "The Trick: Online
-Softmax") -- for every block split, independently of the CUDA path.
+TEST INFRASTRUCTURE ONLY (see oracle/__init__.py).  It lets the tests check the
+method's exactness claim independently of the CUDA path: a result assembled block
+by block equals the materialised softmax result, for every way of cutting the
+query and key axes into blocks (khetwal.com, "FlashAttention: how a memory trick
+unlocked...", section "The Trick: Online Softmax"; the 128-row blocks of the
+section "Tiling" and of the worked example's conceptual listing).
 
-Steps follow "FlashAttention (Conceptual)" in the worked example of
-"FlashAttention: how a memory trick unlocked..." (khetwal.com), in its order:
-outer loop over query blocks, inner loop over key/value blocks, per inner step
-(1) score block, (2) new running max, (3) rescale the output block and the
-normaliser, (4) block probabilities and their row sum, (5) update the
-normaliser, (6) accumulate P V, (7) carry the max; then divide by the
-normaliser.  Readings where the listing is silent or garbled:
-  * the scores carry the scale factor (the score step in "The Quadratic Memory
-    Bottleneck" is written with a scale);
-  * the running max and normaliser are per query row ("for each row ... it
-    maintains two values");
-  * a block in which a row sees no key leaves that row's statistics unchanged
-    (exp(-inf - -inf) is taken as a factor of 1 and the block's P as 0);
-  * the log-sum-exp output is m + ln(normaliser).
+Formulation.  For one query row and any set J of its visible keys, the triple
+
+    m_J = max_{j in J} s_j,   l_J = sum_{j in J} exp(s_j - m_J),
+    a_J = sum_{j in J} exp(s_j - m_J) v_j
+
+is all that is needed from J.  Two disjoint sets combine exactly:
+
+    m = max(m_A, m_B),  w_A = exp(m_A - m),  w_B = exp(m_B - m),
+    l = w_A l_A + w_B l_B,   a = w_A a_A + w_B a_B,
+
+and after all keys O = a / l, LSE = m + ln l.  Folding the key blocks of a query
+block into a running triple, left to right, is the online-softmax recurrence of
+that section (running max, running normaliser, rescaled output).  Readings where
+the pages are silent:
+  * scores carry the scale factor (the score step of "The Quadratic Memory
+    Bottleneck" applies a scale before the softmax);
+  * the triple is kept per query row;
+  * a block in which a row sees no key contributes the empty triple
+    (m = -inf, l = 0, a = 0), whose weight in a merge is 0, so exp(-inf - -inf)
+    is never formed;
+  * a row that sees no key at all gets O = 0 and LSE = -inf.
 """
 from __future__ import annotations
+
+from dataclasses import dataclass
 
 import numpy as np
 
@@ -40,9 +51,56 @@ def visible_mask(n, causal=False, kv_len=None, block_mask=None, tile=128):
     return vis
 
 
+@dataclass
+class RowState:
+    """Per-row summary (m, l, a) of the keys seen so far, for a block of rows."""
+    m: np.ndarray  # [rows] max score, -inf if no key
+    l: np.ndarray  # [rows] sum of exp(score - m)
+    a: np.ndarray  # [rows, d] sum of exp(score - m) * value row
+
+    @staticmethod
+    def empty(rows, d):
+        return RowState(np.full(rows, -np.inf), np.zeros(rows), np.zeros((rows, d)))
+
+
+def _weight(m_part, m_all):
+    """exp(m_part - m_all), and 0 where the part is empty (m_part = -inf)."""
+    out = np.zeros_like(m_part)
+    has = np.isfinite(m_part)
+    out[has] = np.exp(m_part[has] - m_all[has])
+    return out
+
+
+def block_state(scores, values, visible):
+    """State of one key block: `scores` [rows, cols], `values` [cols, d], `visible` mask."""
+    s = np.where(visible, scores, -np.inf)
+    m = s.max(axis=1) if s.shape[1] else np.full(s.shape[0], -np.inf)
+    e = np.zeros_like(s)
+    has = np.isfinite(m)
+    e[has] = np.exp(s[has] - m[has, None])  # masked entries give exp(-inf) = 0
+    return RowState(m, e.sum(axis=1), e @ values)
+
+
+def merge(x: RowState, y: RowState) -> RowState:
+    """Exact combination of the states of two disjoint key sets."""
+    m = np.maximum(x.m, y.m)
+    wx, wy = _weight(x.m, m), _weight(y.m, m)
+    return RowState(m, wx * x.l + wy * y.l, wx[:, None] * x.a + wy[:, None] * y.a)
+
+
+def finish(st: RowState):
+    """(O, LSE) of a final state; rows with no key get O = 0, LSE = -inf."""
+    seen = st.l > 0
+    denom = np.where(seen, st.l, 1.0)
+    o = np.where(seen[:, None], st.a / denom[:, None], 0.0)
+    lse = np.where(seen, st.m + np.log(denom), -np.inf)
+    return o, lse
+
+
 def tiled_attention(q, k, v, scale, block_q, block_k, *, causal=False, kv_len=None,
                     block_mask=None, tile=128):
-    """One head, q/k/v [N, d].  Returns (O [N, d], LSE [N]) in float64."""
+    """One head, q/k/v [N, d]; query blocks of `block_q` rows, key blocks of `block_k`.
+    Returns (O [N, d], LSE [N]) in float64."""
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
@@ -50,37 +108,12 @@ def tiled_attention(q, k, v, scale, block_q, block_k, *, causal=False, kv_len=No
     vis = visible_mask(n, causal, kv_len, block_mask, tile)
     o = np.zeros((n, d))
     lse = np.empty(n)
-    for i0 in range(0, n, block_q):
-        i1 = min(i0 + block_q, n)
-        q_block = q[i0:i1]
-        o_block = np.zeros((i1 - i0, d))
-        running_max = np.full(i1 - i0, -np.inf)
-        running_normalizer = np.zeros(i1 - i0)
-        for j0 in range(0, n, block_k):
-            j1 = min(j0 + block_k, n)
-            k_block, v_block = k[j0:j1], v[j0:j1]
-            # 1. score block (masked entries are -inf)
-            s_block = scale * (q_block @ k_block.T)
-            s_block = np.where(vis[i0:i1, j0:j1], s_block, -np.inf)
-            # 2. new running max
-            local_max = s_block.max(axis=1)
-            new_max = np.maximum(running_max, local_max)
-            # 3. rescale the previous output and normaliser
-            finite = np.isfinite(new_max)
-            safe_max = np.where(finite, new_max, 0.0)
-            factor = np.where(finite, np.exp(running_max - safe_max), 1.0)
-            o_block *= factor[:, None]
-            running_normalizer *= factor
-            # 4. block probabilities and their row sum
-            p_block = np.where(finite[:, None], np.exp(s_block - safe_max[:, None]), 0.0)
-            local_normalizer = p_block.sum(axis=1)
-            # 5. update the normaliser
-            running_normalizer += local_normalizer
-            # 6. accumulate this block's contribution
-            o_block += p_block @ v_block
-            # 7. carry the max
-            running_max = new_max
-        seen = running_normalizer > 0
-        o[i0:i1] = np.where(seen[:, None], o_block / np.where(seen, running_normalizer, 1.0)[:, None], 0.0)
-        lse[i0:i1] = np.where(seen, running_max + np.log(np.where(seen, running_normalizer, 1.0)), -np.inf)
+    for r0 in range(0, n, block_q):
+        r1 = min(r0 + block_q, n)
+        st = RowState.empty(r1 - r0, d)
+        for c0 in range(0, n, block_k):
+            c1 = min(c0 + block_k, n)
+            part = block_state(scale * (q[r0:r1] @ k[c0:c1].T), v[c0:c1], vis[r0:r1, c0:c1])
+            st = merge(st, part)
+        o[r0:r1], lse[r0:r1] = finish(st)
     return o, lse

@@ -214,6 +214,36 @@ def test_tiled_equals_definition_at_page_block_size():
         np.testing.assert_allclose(lse, r["lse"], rtol=1e-12)
 
 
+def test_block_states_merge_in_any_order():
+    # the merge of per-block states is exact, so folding the key blocks in reverse or
+    # pairwise (tree) order gives the same state as the left-to-right fold, and the
+    # empty state (no visible key) leaves a state unchanged
+    from oracle.tiled import RowState, block_state, finish, merge
+    rng = np.random.default_rng(11)
+    n, d = 24, 5
+    q, k, v = 2.0 * _rand(rng, n, d), _rand(rng, n, d), _rand(rng, n, d)
+    vis = visible_mask(n, causal=True)
+    parts = [block_state(0.7 * (q @ k[c:c + 5].T), v[c:c + 5], vis[:, c:c + 5]) for c in range(0, n, 5)]
+    ref = oracle.head_rows(q, k, v, None, 0.7, causal=True)
+    folds = []
+    st = RowState.empty(n, d)
+    for p in parts:
+        st = merge(st, p)
+    folds.append(st)
+    st = RowState.empty(n, d)
+    for p in reversed(parts):
+        st = merge(p, st)
+    folds.append(st)
+    level = parts
+    while len(level) > 1:
+        level = [merge(level[i], level[i + 1]) if i + 1 < len(level) else level[i] for i in range(0, len(level), 2)]
+    folds.append(merge(level[0], RowState.empty(n, d)))
+    for st in folds:
+        o, lse = finish(st)
+        np.testing.assert_allclose(o, ref["o"], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse, ref["lse"], rtol=1e-12, atol=1e-13)
+
+
 # ------------------------------------------------------------ finite differences
 
 @pytest.mark.parametrize("causal,kv_len,use_mask", [(False, None, False), (True, None, False),
