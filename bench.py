@@ -4,22 +4,31 @@
 
 One step = one pass of the whole attention path over one batch of the workload:
 fa_fwd (one kernel) then fa_bwd's three stages (preprocess, main, postprocess),
-inputs resident in HBM.  Each timed step calls the API (--graphs instead captures
-each stage's call once as a CUDA graph after the warm-up and replays the graphs).
-Timed with CUDA events on the launching stream around each step; a second,
-shorter pass puts an event between the stages for the per-kernel times.  L2 is
-flushed between timed steps (512 MiB written, then 256 MiB read so that the
-flush's own dirty lines are written back before the next step).  Max over ranks;
-rank 0 prints one JSON line.
+inputs resident in HBM.  The headline workload is the causal long-context one
+(B1 H32 N65536 d128, 4.3 GB of inputs, far larger than L2); the other workloads
+run as extra legs of the same line, each with its own stage times, roofline and
+clock record.  Each timed step calls the API (--graphs instead captures each
+stage's call once as a CUDA graph after the warm-up and replays the graphs).
+Timed with CUDA events on the launching stream around each step; a second pass
+puts an event between the stages for the per-kernel times.  L2 is flushed
+between timed steps (512 MiB written, then 256 MiB read so that the flush's own
+dirty lines are written back before the next step).  Max over ranks; rank 0
+prints one JSON line.
 
 FLOP convention: forward 4*B*H*N^2*d (halved when causal), backward 2.5x forward;
-`value` is forward+backward TFLOP/s.  The roofline object reports the dominant
-kernel against the measured dense bf16 peak, with achieved FLOPs counted over the
-128x128 tile pairs the kernel actually visits (4*128*128*d per pair forward,
-10*128*128*d backward).
+`value` is forward+backward TFLOP/s.  Beside it: "algorithmic" FLOPs count the
+128x128 tile pairs the kernels visit (4*128*128*d per pair forward, 10*128*128*d
+backward), "useful" FLOPs the visible query/key pairs only (4*d per pair forward,
+14*d forward+backward).  The roofline object reports the dominant kernel against
+the measured dense bf16 peak.
 
---impl reference times the fp64 CPU oracle on the host cores instead (one head of
-the workload per step), as the reference arm.
+nvidia-smi is polled every 200 ms for the whole run; each leg reports the median
+SM clock and the throttle reasons seen during its own timed region.
+
+--impl reference times the fp64 CPU oracle on the host cores instead, as the
+reference arm: each step is the oracle's row pass over a seeded sample of query
+rows of the workload's first head, and the whole-workload time is extrapolated
+from it by visible pair count.
 """
 from __future__ import annotations
 
@@ -62,7 +71,10 @@ class L2Flush:
         self.w.zero_()
         self.torch.sum(self.r, dim=0, out=self.acc)
 TILE = 128
-EXTRA_WORKLOAD = "long_causal_16k"
+HEADLINE_WORKLOAD = "long_causal_64k"
+EXTRA_WORKLOADS = ("long_causal_16k", "gpt2_causal", "block_sparse_8k", "bert_large_padded")
+FP8_WORKLOAD = "long_causal_16k"
+EXTRA_MIN_SECONDS = 1.0   # an extra leg's timed region lasts at least this long (clock samples)
 
 
 # ------------------------------------------------------------------ host logic
@@ -92,6 +104,32 @@ def visited_tile_pairs(N, causal, kv_len, block_mask, B, H):
 
 def algorithmic_flops(pairs, d):
     return {"fwd": pairs * 4.0 * TILE * TILE * d, "bwd": pairs * 10.0 * TILE * TILE * d}
+
+
+def row_visible_counts(N, rows, causal, kv_len, block_mask, tile=TILE):
+    """Number of keys each query row in `rows` sees (one sequence: kv_len an int or None)."""
+    rows = np.asarray(rows, np.int64)
+    lim = np.full(rows.shape, N if kv_len is None else min(max(int(kv_len), 0), N), np.int64)
+    if causal:
+        lim = np.minimum(lim, rows + 1)
+    if block_mask is None:
+        return lim
+    bm = np.asarray(block_mask).astype(bool)
+    counts = np.zeros(rows.shape, np.int64)
+    for tj in range((N + tile - 1) // tile):
+        width = np.clip(np.minimum(lim, min(N, (tj + 1) * tile)) - tj * tile, 0, None)
+        counts += np.where(bm[rows // tile, tj], width, 0)
+    return counts
+
+
+def useful_score_pairs(N, causal, kv_len, block_mask, B, H):
+    """Visible (query, key) pairs summed over heads: the scores the method must compute."""
+    rows = np.arange(N)
+    total = 0
+    for b in range(B):
+        kl = None if kv_len is None else int(kv_len[b])
+        total += int(row_visible_counts(N, rows, causal, kl, block_mask).sum()) * H
+    return total
 
 
 def splitkv_work(B, H, Nq, Nk, d):
@@ -166,39 +204,48 @@ def aggregate_line(per_rank_flops, world, max_ms_step, steps):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    """Polls nvidia-smi (SM clock, max clock, power, throttle reasons) every `period`
+    seconds on a background thread for the whole run; `window(t0, t1)` summarises the
+    samples taken between two time.monotonic() stamps."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, period=0.2):
+        import threading
         self.gpu_index = gpu_index
-        self.proc = None
+        self.period = period
+        self.samples = []  # (monotonic time of the query's midpoint, csv line)
+        self._stop = threading.Event()
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self.available = True
 
-    def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-i", str(self.gpu_index), "-lms", "200"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+    def _run(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-i", str(self.gpu_index)]
+        while not self._stop.is_set():
+            t0 = time.monotonic()
+            try:
+                out = subprocess.run(cmd, capture_output=True, text=True, timeout=5).stdout
+            except (OSError, subprocess.SubprocessError):
+                self.available = False
+                return
+            t1 = time.monotonic()
+            for ln in out.splitlines():
+                if ln.strip():
+                    self.samples.append((0.5 * (t0 + t1), ln))
+            self._stop.wait(max(0.0, self.period - (t1 - t0)))
+
+    def start(self):
+        self._thread.start()
         return self
 
-    def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
-        return False
+    def stop(self):
+        self._stop.set()
+        self._thread.join(timeout=10)
 
-    def summary(self):
-        return parse_clock_lines(getattr(self, "lines", []))
+    def window(self, t0, t1):
+        return parse_clock_lines([ln for t, ln in list(self.samples) if t0 <= t <= t1])
 
 
 def parse_clock_lines(lines):
@@ -232,11 +279,13 @@ def device_inputs(inp, torch):
     return t
 
 
-def time_workload(name, steps, warmup, torch, fa, flush, dist=None, sampler=None, override=None, graphs=False):
-    """Run `steps` timed fwd+bwd steps on one workload; per-stage CUDA-event times.
+def time_workload(name, steps, warmup, torch, fa, flush, dist=None, override=None, graphs=False, min_seconds=0.0):
+    """Run timed fwd+bwd steps on one workload; per-stage CUDA-event times.
 
-    With `graphs`, each stage's API call is captured once as a CUDA graph after the
-    warm-up and the timed steps replay the graphs (same kernels, same arguments)."""
+    Exactly `steps` timed steps, or more if `min_seconds` asks for a longer timed
+    region (the extra legs, so that the clock sampler sees them).  With `graphs`,
+    each stage's API call is captured once as a CUDA graph after the warm-up and the
+    timed steps replay the graphs (same kernels, same arguments)."""
     spec = inputs.WORKLOADS[name]
     inp = inputs.workload_inputs(name, **(override or {}))
     B, H, N, d = inp.q.shape
@@ -265,12 +314,15 @@ def time_workload(name, steps, warmup, torch, fa, flush, dist=None, sampler=None
         if ev is not None:
             ev[len(launch)].record(stream)
 
+    torch.cuda.synchronize()
+    tw = time.perf_counter()
     for _ in range(warmup):
         flush()
         step()
+    torch.cuda.synchronize()
+    warm_step_s = (time.perf_counter() - tw) / max(1, warmup)
     launch_mode = "api calls"
     if graphs:
-        torch.cuda.synchronize()
         try:
             captured = []
             for fn in stages:
@@ -287,23 +339,25 @@ def time_workload(name, steps, warmup, torch, fa, flush, dist=None, sampler=None
         for _ in range(2):
             flush()
             step()
+    if min_seconds > 0:
+        steps = max(steps, min(5000, math.ceil(min_seconds / max(warm_step_s, 1e-6))))
     # Timed steps: one event pair around each step.  The four launches of a step run
     # back to back, so each kernel's launch overlaps the tail of the one before it.
     step_events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     if dist is not None and dist.is_initialized():
         dist.barrier()
     torch.cuda.synchronize()
-    ctx = sampler if sampler is not None else _Null()
-    with ctx:
-        t0 = time.perf_counter()
-        for i in range(steps):
-            flush()
-            step_events[i][0].record(stream)
-            step()
-            step_events[i][1].record(stream)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
-    # Stage breakdown: a shorter pass with an event between the stages (which
+    t0 = time.perf_counter()
+    m0 = time.monotonic()
+    for i in range(steps):
+        flush()
+        step_events[i][0].record(stream)
+        step()
+        step_events[i][1].record(stream)
+    torch.cuda.synchronize()
+    m1 = time.monotonic()
+    wall = time.perf_counter() - t0
+    # Stage breakdown: a second pass with an event between the stages (which
     # serialises them), for the per-kernel times and the roofline.
     n_stage = max(3, min(steps, 100))
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_stage)]
@@ -325,14 +379,92 @@ def time_workload(name, steps, warmup, torch, fa, flush, dist=None, sampler=None
     ms["step"] = sum(ev[0].elapsed_time(ev[1]) for ev in step_events) / steps
     ms["wall_s"] = wall
     ms["launch"] = launch_mode
+    ms["steps"] = steps
+    ms["window"] = (m0, m1)
     pairs = visited_tile_pairs(N, causal, inp.kv_len, inp.block_mask, B, H)
-    return inp, ms, pairs, (q, k, v, do, bm, kl)
+    return inp, ms, pairs
 
 
-def time_fp8_forward(name, steps, warmup, torch, fa, flush):
+def leg_report(inp, ms, pairs, peaks, clocks):
+    """Throughput, fractions of peak and the roofline of one timed workload."""
+    B, H, N, d = inp.q.shape
+    causal = inp.causal
+    f = formula_fwd_flops(B, H, N, d, causal)
+    alg = algorithmic_flops(pairs, d)
+    useful = useful_score_pairs(N, causal, inp.kv_len, inp.block_mask, B, H) * 4.0 * d
+    bwd_ms = ms["bwd_preprocess"] + ms["bwd_main"] + ms["bwd_postprocess"]
+    burst = peaks["bf16_tflops"]
+
+    def tf(flops, t_ms):
+        return flops / (t_ms * 1e-3) / 1e12
+
+    kern = {"fwd": (ms["fwd"], alg["fwd"]), "bwd_main": (ms["bwd_main"], alg["bwd"])}
+    dom = max(kern, key=lambda k2: kern[k2][0])
+    achieved = tf(kern[dom][1], kern[dom][0])
+    long_step = ms["step"] >= 5.0
+    rep = {
+        "config": {"B": B, "H": H, "N": N, "d": d, "causal": causal, "key_padding": inp.kv_len is not None,
+                   "block_mask": inp.block_mask is not None, "seed": inp.seed},
+        "fwd_tflops": round(tf(f, ms["fwd"]), 2),
+        "bwd_tflops": round(tf(2.5 * f, bwd_ms), 2),
+        "fwd_bwd_tflops": round(tf(3.5 * f, ms["step"]), 2),
+        "fwd_frac_of_peak": round(tf(f, ms["fwd"]) / burst, 4),
+        "bwd_frac_of_peak": round(tf(2.5 * f, bwd_ms) / burst, 4),
+        "bwd_main_frac_of_peak": round(tf(alg["bwd"], ms["bwd_main"]) / burst, 4),
+        "fwd_bwd_frac_of_peak": round(tf(3.5 * f, ms["step"]) / burst, 4),
+        "algorithmic_tflops": {"fwd": round(tf(alg["fwd"], ms["fwd"]), 2),
+                               "bwd_main": round(tf(alg["bwd"], ms["bwd_main"]), 2)},
+        "useful_tflops": {"fwd": round(tf(useful, ms["fwd"]), 2),
+                          "fwd_bwd": round(tf(3.5 * useful, ms["step"]), 2)},
+        "stage_ms": {k2: round(v2, 5) for k2, v2 in ms.items() if k2 not in ("wall_s", "launch", "steps", "window")},
+        "timed_steps": ms["steps"],
+        "flops_per_step": {"formula_fwd": f, "formula_fwd_bwd": 3.5 * f, "visited_tile_pairs": pairs,
+                           "algorithmic_fwd": alg["fwd"], "algorithmic_bwd": alg["bwd"],
+                           "useful_fwd": useful, "useful_fwd_bwd": 3.5 * useful},
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2), "peak": burst,
+                     "unit": "TFLOP/s", "frac": round(achieved / burst, 4), "traffic": None,
+                     "peak_source": f"bf16_tflops burst, {peaks['source']}"},
+        "clocks": clocks,
+    }
+    if long_step:
+        sus = peaks["bf16_tflops_sustained"]
+        rep["roofline"]["frac_of_sustained"] = round(achieved / sus, 4)
+        rep["roofline"]["peak_sustained"] = sus
+    return rep
+
+
+def _timed_loop(run, steps, warmup, torch, fa, flush, stream, min_seconds=0.0):
+    """Warm up, then time `run` once per step (L2 flushed between steps, one event pair
+    per step on the launching stream), for `steps` steps or at least `min_seconds`.
+    Returns (mean ms per call, monotonic window of the timed region)."""
+    torch.cuda.synchronize()
+    tw = time.perf_counter()
+    for _ in range(warmup):
+        flush()
+        run()
+    torch.cuda.synchronize()
+    if min_seconds > 0:
+        per = (time.perf_counter() - tw) / max(1, warmup)
+        steps = max(steps, min(20000, math.ceil(min_seconds / max(per, 1e-6))))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    m0 = time.monotonic()
+    for i in range(steps):
+        flush()
+        ev[i][0].record(stream)
+        run()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    m1 = time.monotonic()
+    if fa.fa_get_device_status() != 0:
+        raise RuntimeError("device status reports a timed-out wait")
+    return sum(e[0].elapsed_time(e[1]) for e in ev) / steps, (m0, m1)
+
+
+def time_fp8_forward(name, steps, warmup, torch, fa, flush, min_seconds=0.0):
     """fa_fwd_fp8 on the E4M3 version of a workload (one launch per step, L2 flushed
     between steps, one event pair per step on the launching stream).  Returns
-    (inputs, mean ms per launch)."""
+    (inputs, mean ms per launch, timed window)."""
     inp = inputs.workload_fp8_inputs(name)
     B, H, N, d = inp.q8.shape
     dev = {n: torch.from_numpy(np.ascontiguousarray(getattr(inp, n))).cuda() for n in ("q8", "k8", "vt8")}
@@ -346,26 +478,14 @@ def time_fp8_forward(name, steps, warmup, torch, fa, flush):
         fa.fa_fwd_fp8(dev["q8"], dev["k8"], dev["vt8"], o, lse, inp.scale, inp.descale_q, inp.descale_k,
                       inp.descale_v, inp.causal, bm, kl, stream)
 
-    for _ in range(warmup):
-        flush()
-        run()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
-    torch.cuda.synchronize()
-    for i in range(steps):
-        flush()
-        ev[i][0].record(stream)
-        run()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    if fa.fa_get_device_status() != 0:
-        raise RuntimeError("device status reports a timed-out wait")
-    return inp, sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    ms, window = _timed_loop(run, steps, warmup, torch, fa, flush, stream, min_seconds)
+    return inp, ms, window
 
 
-def time_splitkv(name, steps, warmup, torch, fa, flush):
+def time_splitkv(name, steps, warmup, torch, fa, flush, min_seconds=0.0):
     """fa_fwd_splitkv on a query block / key cache workload (automatic split count; both
     launches of the call inside each event pair; L2 flushed between steps).  Returns
-    (inputs, n_splits, mean ms per call)."""
+    (inputs, n_splits, mean ms per call, timed window)."""
     inp = inputs.qk_workload_inputs(name)
     B, H, Nq, d = inp.q.shape
     Nk = inp.k.shape[2]
@@ -383,28 +503,8 @@ def time_splitkv(name, steps, warmup, torch, fa, flush):
     def run():
         fa.fa_fwd_splitkv(q, k, v, o, lse, inp.scale, None, n_splits, ws, stream)
 
-    for _ in range(warmup):
-        flush()
-        run()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
-    torch.cuda.synchronize()
-    for i in range(steps):
-        flush()
-        ev[i][0].record(stream)
-        run()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    if fa.fa_get_device_status() != 0:
-        raise RuntimeError("device status reports a timed-out wait")
-    return inp, n_splits, sum(e[0].elapsed_time(e[1]) for e in ev) / steps
-
-
-class _Null:
-    def __enter__(self):
-        return self
-
-    def __exit__(self, *a):
-        return False
+    ms, window = _timed_loop(run, steps, warmup, torch, fa, flush, stream, min_seconds)
+    return inp, n_splits, ms, window
 
 
 def e2e_throughput(inp, steps, torch, fa, depth=2):
@@ -492,26 +592,67 @@ def e2e_throughput(inp, steps, torch, fa, depth=2):
     return ms, h2d, d2h
 
 
-def cpu_baseline_sample(name, budget_s=20.0):
-    """The fp64 oracle, as it stands, on the host cores over a bounded sample of heads."""
+def oracle_row_sample(inp, n_rows, seed, nthreads=0):
+    """The fp64 oracle's row pass (O, LSE, D and dQ) over `n_rows` seeded query rows of
+    head (0, 0).  Returns (seconds, visible pairs processed)."""
     import oracle
-    inp = inputs.workload_inputs(name)
-    B, H, N, d = inp.q.shape
-    heads = [(b, h) for b in range(B) for h in range(H)]
-    done = 0
+    N = inp.q.shape[2]
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(N, size=min(n_rows, N), replace=False)).astype(np.int32)
+    kl = None if inp.kv_len is None else int(inp.kv_len[0])
     t0 = time.perf_counter()
-    for b, h in heads:
-        oracle.attention_backward(inp.q[b:b + 1, h:h + 1], inp.k[b:b + 1, h:h + 1], inp.v[b:b + 1, h:h + 1],
-                                  inp.dout[b:b + 1, h:h + 1], inp.scale, causal=inp.causal,
-                                  kv_len=None if inp.kv_len is None else inp.kv_len[b:b + 1],
-                                  block_mask=inp.block_mask)
-        done += 1
-        if time.perf_counter() - t0 > budget_s:
-            break
+    oracle.head_rows(inp.q[0, 0], inp.k[0, 0], inp.v[0, 0], inp.dout[0, 0], inp.scale, causal=inp.causal,
+                     kv_len=kl, block_mask=inp.block_mask, rows=rows, nthreads=nthreads)
     dt = time.perf_counter() - t0
-    flops = 3.5 * formula_fwd_flops(1, done, N, d, inp.causal)
-    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.default_threads(), "kind": "oracle",
-            "sample": f"fp64 oracle fwd+bwd on {done} of {B * H} heads of {name} ({dt:.1f} s)"}
+    return dt, int(row_visible_counts(N, rows, inp.causal, kl, inp.block_mask).sum())
+
+
+def extrapolated_oracle_seconds(sample_s, sample_pairs, total_pairs):
+    """Whole-workload fp64 oracle time from a row-pass sample.  The oracle's column
+    pass (dK, dV) does the same vector work per visible pair as its row pass (two dot
+    products and two axpys of length d), so the whole forward+backward takes about
+    twice the row pass, and the row pass scales with the visible pairs."""
+    return 2.0 * sample_s * total_pairs / max(sample_pairs, 1)
+
+
+def cpu_baseline_sample(name, n_rows=2048):
+    """The fp64 oracle, as it stands, on the host cores: a seeded row sample of the
+    workload's first head, extrapolated to the whole workload; plus one-thread times
+    of the small workloads."""
+    import oracle
+    full = inputs.WORKLOADS[name]
+    B, H, N, d = full["B"], full["H"], full["N"], full["d"]
+    # the generator fills [B, H, N, d] in C order, so with H = 1 head (0, 0) is the full
+    # workload's first head, and the key lengths (one per sequence) are the same
+    inp = inputs.workload_inputs(name, H=1)
+    dt, pairs = oracle_row_sample(inp, n_rows, seed=0)
+    total_pairs = useful_score_pairs(N, inp.causal, inp.kv_len, inp.block_mask, B, H)
+    t_all = extrapolated_oracle_seconds(dt, pairs, total_pairs)
+    flops = 3.5 * formula_fwd_flops(B, H, N, d, inp.causal)
+    threads = oracle.default_threads()
+    res = {"value": flops / t_all / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+           "sample": (f"fp64 oracle row pass (O, LSE, dQ) on {min(n_rows, N)} seeded query rows of head (0,0) of "
+                      f"{name}: {dt:.2f} s measured for {pairs:.3g} visible pairs; whole workload "
+                      f"({total_pairs:.3g} pairs, forward+backward with the column pass counted at the row pass's "
+                      f"per-pair cost) extrapolated to {t_all:.0f} s on {threads} threads"),
+           "measured_s": round(dt, 3), "extrapolated_s": round(t_all, 1)}
+    one = {}
+    for small in ("tiny_fp32", "bert_large_padded", "gpt2_causal"):
+        s_inp = inputs.workload_inputs(small, H=1) if small != "tiny_fp32" else inputs.workload_inputs(small)
+        sB, _, sN, sd = s_inp.q.shape
+        t0 = time.perf_counter()
+        if small == "tiny_fp32":
+            oracle.attention_forward(s_inp.q, s_inp.k, s_inp.v, s_inp.scale, nthreads=1)
+            fl, what = formula_fwd_flops(1, 1, sN, sd, False), "forward, the whole workload"
+        else:
+            kl = None if s_inp.kv_len is None else s_inp.kv_len[:1]
+            oracle.attention_backward(s_inp.q[:1, :1], s_inp.k[:1, :1], s_inp.v[:1, :1], s_inp.dout[:1, :1],
+                                      s_inp.scale, causal=s_inp.causal, kv_len=kl, nthreads=1)
+            fl, what = 3.5 * formula_fwd_flops(1, 1, sN, sd, s_inp.causal), "forward+backward, head (0,0)"
+        dt1 = time.perf_counter() - t0
+        one[small] = {"tflops": fl / dt1 / 1e12, "seconds": round(dt1, 4), "what": what}
+    res["one_thread"] = one
+    return res
 
 
 def run_ours(args):
@@ -527,98 +668,102 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     fa.load()
     flush = L2Flush(torch)
-    sampler = ClockSampler(local)
-    inp, ms, pairs, _ = time_workload(args.workload, args.steps, args.warmup, torch, fa, flush,
-                                      dist if world > 1 else None, sampler, graphs=args.graphs)
-    B, H, N, d = inp.q.shape
-    causal = inputs.WORKLOADS[args.workload]["causal"]
-    fwd_formula = formula_fwd_flops(B, H, N, d, causal)
-    step_ms = reduce_max_over_ranks(ms["step"], dist if world > 1 else None)
-    fwd_ms = reduce_max_over_ranks(ms["fwd"], dist if world > 1 else None)
-    value = aggregate_line(3.5 * fwd_formula, world, step_ms, args.steps)
-    fwd_tflops = aggregate_line(fwd_formula, world, fwd_ms, args.steps)
+    sampler = ClockSampler(local).start()
     peaks = load_peaks()
-    alg = algorithmic_flops(pairs, d)
-    kern = {"fwd": (ms["fwd"], alg["fwd"]), "bwd_main": (ms["bwd_main"], alg["bwd"])}
-    dom = max(kern, key=lambda k2: kern[k2][0])
-    dur_ms, flops = kern[dom]
-    achieved = flops / (dur_ms * 1e-3) / 1e12
-    traffic = recorded_traffic(dom, args.workload)
-    clocks = sampler.summary()
-
-    line = {
-        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d, "causal": causal,
-                   "key_padding": inp.kv_len is not None, "block_mask": inp.block_mask is not None,
-                   "seed": inp.seed, "l2": "flushed between timed steps (512 MiB written, 256 MiB read)",
-                   "launch": ms["launch"],
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "fwd_tflops": round(fwd_tflops, 3),
-        "fwd_frac_of_peak": round(fwd_tflops / peaks["bf16_tflops"], 4),
-        "fwd_bwd_frac_of_peak": round(value / world / peaks["bf16_tflops"], 4),
-        "stage_ms": {k2: round(v2, 5) for k2, v2 in ms.items() if k2 not in ("wall_s", "launch")},
-        "wall_ms_per_step": round(ms["wall_s"] / args.steps * 1e3, 5),
-        "flops_per_step": {"formula_fwd": fwd_formula, "formula_fwd_bwd": 3.5 * fwd_formula,
-                           "visited_tile_pairs": pairs, "algorithmic_fwd": alg["fwd"], "algorithmic_bwd": alg["bwd"]},
-        "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
-                     "peak_source": f"bf16_tflops burst, {peaks['source']}"},
-        "gpu_launches": 4 * args.steps,
-        "clocks": clocks,
-    }
-    if rank == 0 and world == 1 and not args.no_e2e:
-        e2e_ms, h2d, d2h = e2e_throughput(inp, max(10, min(args.steps, 200)), torch, fa)
-        line["e2e"] = {"value": round(3.5 * fwd_formula / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
-                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)}
-    if rank == 0 and world == 1 and not args.no_extra and args.workload != EXTRA_WORKLOAD:
-        xin, xms, xpairs, _ = time_workload(EXTRA_WORKLOAD, max(3, min(args.steps, 10)), 3, torch, fa, flush,
-                                            graphs=args.graphs)
-        xB, xH, xN, xd = xin.q.shape
-        xf = formula_fwd_flops(xB, xH, xN, xd, True)
-        xbwd_ms = xms["bwd_preprocess"] + xms["bwd_main"] + xms["bwd_postprocess"]
-        line["long_causal_16k"] = {
-            "fwd_tflops": round(xf / (xms["fwd"] * 1e-3) / 1e12, 2),
-            "bwd_tflops": round(2.5 * xf / (xbwd_ms * 1e-3) / 1e12, 2),
-            "fwd_frac_of_peak": round(xf / (xms["fwd"] * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-            "bwd_frac_of_peak": round(2.5 * xf / (xbwd_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-            "stage_ms": {k2: round(v2, 4) for k2, v2 in xms.items() if k2 not in ("wall_s", "launch")},
+    extra = rank == 0 and world == 1 and not args.no_extra
+    try:
+        inp, ms, pairs = time_workload(args.workload, args.steps, args.warmup, torch, fa, flush,
+                                       dist if world > 1 else None, graphs=args.graphs)
+        B, H, N, d = inp.q.shape
+        causal = inp.causal
+        fwd_formula = formula_fwd_flops(B, H, N, d, causal)
+        step_ms = reduce_max_over_ranks(ms["step"], dist if world > 1 else None)
+        fwd_ms = reduce_max_over_ranks(ms["fwd"], dist if world > 1 else None)
+        value = aggregate_line(3.5 * fwd_formula, world, step_ms, args.steps)
+        rep = leg_report(inp, ms, pairs, peaks, sampler.window(*ms["window"]))
+        rep["roofline"]["traffic"] = recorded_traffic(rep["roofline"]["kernel"], args.workload)
+        bwd_ms = ms["bwd_preprocess"] + ms["bwd_main"] + ms["bwd_postprocess"]
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, **rep["config"],
+                       "l2": "flushed between timed steps (512 MiB written, 256 MiB read)",
+                       "launch": ms["launch"],
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "fwd_tflops": round(aggregate_line(fwd_formula, world, fwd_ms, args.steps), 3),
+            "bwd_tflops": rep["bwd_tflops"],
+            "fwd_frac_of_peak": rep["fwd_frac_of_peak"],
+            "bwd_frac_of_peak": rep["bwd_frac_of_peak"],
+            "bwd_main_frac_of_peak": rep["bwd_main_frac_of_peak"],
+            "fwd_bwd_frac_of_peak": round(value / world / peaks["bf16_tflops"], 4),
+            "peak_tflops": {"burst": peaks["bf16_tflops"], "sustained": peaks["bf16_tflops_sustained"],
+                            "source": peaks["source"]},
+            "stage_ms": rep["stage_ms"],
+            "bwd_ms": round(bwd_ms, 5),
+            "wall_ms_per_step": round(ms["wall_s"] / args.steps * 1e3, 5),
+            "flops_per_step": rep["flops_per_step"],
+            "algorithmic_tflops": rep["algorithmic_tflops"],
+            "useful_tflops": rep["useful_tflops"],
+            "roofline": rep["roofline"],
+            "gpu_launches": 4 * args.steps,
+            "clocks": rep["clocks"],
         }
-    if rank == 0 and world == 1 and not args.no_extra:
-        finp, fms = time_fp8_forward(EXTRA_WORKLOAD, max(3, min(args.steps, 10)), 3, torch, fa, flush)
-        fB, fH, fN, fd = finp.q8.shape
-        ff = formula_fwd_flops(fB, fH, fN, fd, finp.causal)
-        fpairs = visited_tile_pairs(fN, finp.causal, finp.kv_len, finp.block_mask, fB, fH)
-        fach = algorithmic_flops(fpairs, fd)["fwd"] / (fms * 1e-3) / 1e12
-        fp8_peak = 2.0 * peaks["bf16_tflops"]
-        line["fp8_forward"] = {
-            "workload": EXTRA_WORKLOAD, "dtype": "e4m3 in, fp32 accumulate, bf16 out",
-            "tflops": round(ff / (fms * 1e-3) / 1e12, 2), "ms": round(fms, 4),
-            "roofline": {"kernel": "fwd_fp8", "bound": "tensor", "achieved": round(fach, 2),
-                         "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(fach / fp8_peak, 4),
-                         "traffic": recorded_traffic("fwd_fp8", EXTRA_WORKLOAD),
-                         "peak_source": f"bf16_tflops burst ({peaks['source']}) x 2, the nominal dense "
-                                        "fp8:bf16 ratio (4.5 : 2.25 PFLOP/s)"},
-        }
-    if rank == 0 and world == 1 and not args.no_extra:
-        line["split_kv"] = {}
-        for qk_name in sorted(inputs.QK_WORKLOADS):
-            sin, n_splits, sms = time_splitkv(qk_name, max(3, min(args.steps, 20)), 3, torch, fa, flush)
-            sB, sH, sNq, sd = sin.q.shape
-            sNk = sin.k.shape[2]
-            flops, nbytes = splitkv_work(sB, sH, sNq, sNk, sd)
-            gbs = nbytes / (sms * 1e-3) / 1e9
-            line["split_kv"][qk_name] = {
-                "config": {"B": sB, "H": sH, "Nq": sNq, "Nk": sNk, "d": sd, "n_splits": n_splits},
-                "ms": round(sms, 4), "tflops": round(flops / (sms * 1e-3) / 1e12, 2),
-                "roofline": {"kernel": "fwd_splitkv + combine (one call)", "bound": "hbm", "achieved": round(gbs, 1),
-                             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                             "traffic": recorded_traffic("fwd_splitkv", qk_name),
-                             "algorithmic_bytes": "Q, K, V read once, O (bf16) and LSE written"},
+        if rank == 0 and world == 1 and not args.no_e2e:
+            e2e_ms, h2d, d2h = e2e_throughput(inp, max(10, min(args.steps, 200)), torch, fa)
+            line["e2e"] = {"value": round(3.5 * fwd_formula / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+                           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)}
+        del inp
+        if extra:
+            line["extras"] = {}
+            for name in EXTRA_WORKLOADS:
+                if name == args.workload:
+                    continue
+                xin, xms, xpairs = time_workload(name, 10, 3, torch, fa, flush, graphs=args.graphs,
+                                                 min_seconds=EXTRA_MIN_SECONDS)
+                xrep = leg_report(xin, xms, xpairs, peaks, sampler.window(*xms["window"]))
+                xrep["roofline"]["traffic"] = recorded_traffic(xrep["roofline"]["kernel"], name)
+                line["extras"][name] = xrep
+            finp, fms, fwin = time_fp8_forward(FP8_WORKLOAD, 10, 3, torch, fa, flush, min_seconds=EXTRA_MIN_SECONDS)
+            fB, fH, fN, fd = finp.q8.shape
+            ff = formula_fwd_flops(fB, fH, fN, fd, finp.causal)
+            fpairs = visited_tile_pairs(fN, finp.causal, finp.kv_len, finp.block_mask, fB, fH)
+            fach = algorithmic_flops(fpairs, fd)["fwd"] / (fms * 1e-3) / 1e12
+            fp8_peak = 2.0 * peaks["bf16_tflops"]
+            line["fp8_forward"] = {
+                "workload": FP8_WORKLOAD, "dtype": "e4m3 in, fp32 accumulate, bf16 out",
+                "tflops": round(ff / (fms * 1e-3) / 1e12, 2), "ms": round(fms, 4),
+                "roofline": {"kernel": "fwd_fp8", "bound": "tensor", "achieved": round(fach, 2),
+                             "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(fach / fp8_peak, 4),
+                             "traffic": recorded_traffic("fwd_fp8", FP8_WORKLOAD),
+                             "peak_source": f"ASSUMED, not measured: bf16_tflops burst ({peaks['source']}) x 2, "
+                                            "the nominal dense fp8:bf16 ratio (4.5 : 2.25 PFLOP/s)"},
+                "clocks": sampler.window(*fwin),
             }
+            del finp
+            line["split_kv"] = {}
+            for qk_name in sorted(inputs.QK_WORKLOADS):
+                sin, n_splits, sms, swin = time_splitkv(qk_name, 20, 3, torch, fa, flush,
+                                                        min_seconds=EXTRA_MIN_SECONDS)
+                sB, sH, sNq, sd = sin.q.shape
+                sNk = sin.k.shape[2]
+                flops, nbytes = splitkv_work(sB, sH, sNq, sNk, sd)
+                gbs = nbytes / (sms * 1e-3) / 1e9
+                line["split_kv"][qk_name] = {
+                    "config": {"B": sB, "H": sH, "Nq": sNq, "Nk": sNk, "d": sd, "n_splits": n_splits},
+                    "ms": round(sms, 4), "tflops": round(flops / (sms * 1e-3) / 1e12, 2),
+                    "roofline": {"kernel": "fwd_splitkv + combine (one call)", "bound": "hbm",
+                                 "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                 "frac": round(gbs / peaks["hbm_gbs"], 4),
+                                 "traffic": recorded_traffic("fwd_splitkv", qk_name),
+                                 "algorithmic_bytes": "Q, K, V read once, O (bf16) and LSE written"},
+                    "clocks": sampler.window(*swin),
+                }
+                del sin
+    finally:
+        sampler.stop()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_sample(args.workload, args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline_sample(args.workload, args.cpu_rows)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -626,37 +771,39 @@ def run_ours(args):
 
 
 def run_reference(args):
-    """The oracle as the reference arm: one head of the workload per step on the host cores."""
+    """The oracle as the reference arm, on the host cores: each step is the row pass
+    over a seeded sample of query rows of the workload's first head; the rate is the
+    whole workload's convention FLOPs over its extrapolated oracle time."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1 and rank != 0:
         return
     import oracle
-    inp = inputs.workload_inputs(args.workload)
-    B, H, N, d = inp.q.shape
-    heads = [(b, h) for b in range(B) for h in range(H)]
-
-    def step(i):
-        b, h = heads[i % len(heads)]
-        oracle.attention_backward(inp.q[b:b + 1, h:h + 1], inp.k[b:b + 1, h:h + 1], inp.v[b:b + 1, h:h + 1],
-                                  inp.dout[b:b + 1, h:h + 1], inp.scale, causal=inp.causal,
-                                  kv_len=None if inp.kv_len is None else inp.kv_len[b:b + 1],
-                                  block_mask=inp.block_mask)
-
+    full = inputs.WORKLOADS[args.workload]
+    B, H, N, d = full["B"], full["H"], full["N"], full["d"]
+    inp = inputs.workload_inputs(args.workload, H=1)
+    kv_len = inp.kv_len
+    total_pairs = useful_score_pairs(N, inp.causal, kv_len, inp.block_mask, B, H)
     for i in range(args.warmup):
-        step(i)
+        oracle_row_sample(inp, args.ref_rows, seed=i)
+    t_sum, pairs_sum = 0.0, 0
     t0 = time.perf_counter()
     for i in range(args.steps):
-        step(args.warmup + i)
-    dt = time.perf_counter() - t0
-    flops = 3.5 * formula_fwd_flops(1, 1, N, d, inp.causal) * args.steps
-    value = flops / dt / 1e12
-    sample = f"fp64 oracle fwd+bwd, one head of {args.workload} per step ({args.steps} steps, {dt:.1f} s)"
+        dt, pairs = oracle_row_sample(inp, args.ref_rows, seed=args.warmup + i)
+        t_sum += dt
+        pairs_sum += pairs
+    wall = time.perf_counter() - t0
+    t_all = extrapolated_oracle_seconds(t_sum, pairs_sum, total_pairs)
+    value = 3.5 * formula_fwd_flops(B, H, N, d, inp.causal) / t_all / 1e12
+    sample = (f"fp64 oracle row pass (O, LSE, dQ) on {min(args.ref_rows, N)} seeded query rows of head (0,0) of "
+              f"{args.workload} per step ({args.steps} steps, {wall:.1f} s, {pairs_sum:.3g} visible pairs); whole "
+              f"workload ({total_pairs:.3g} pairs, forward+backward with the column pass counted at the row pass's "
+              f"per-pair cost) extrapolated to {t_all:.0f} s")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d,
-                       "sample": "one head per step, cycling over all heads"},
+            "config": {"workload": args.workload, "B": B, "H": H, "N": N, "d": d, "causal": inp.causal,
+                       "sample": f"{min(args.ref_rows, N)} seeded query rows of head (0,0) per step"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.default_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -666,15 +813,16 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="bert_large_padded", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=HEADLINE_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--graphs", action="store_true", help="replay one CUDA graph per stage instead of calling the API")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--cpu-rows", type=int, default=2048, help="query rows the cpu_baseline oracle sample covers")
+    ap.add_argument("--ref-rows", type=int, default=1024, help="query rows per reference-arm step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -99,3 +99,39 @@ def test_splitkv_work_counts():
     kv = 2 * 256 * 32768 * 128 * 2          # K and V in bf16
     assert nbytes == kv + 2 * 256 * 128 * 2 + 256 * 4  # + Q and O rows in bf16, LSE in fp32
     assert abs(kv - 4.295e9) < 1e6           # the 4.30 GB the traffic capture reads
+
+
+def test_visible_counts_match_the_element_mask():
+    from oracle.tiled import visible_mask
+    rng = np.random.default_rng(3)
+    n, tile = 45, 8
+    T = (n + tile - 1) // tile
+    bm = (rng.random((T, T)) < 0.5).astype(np.uint8)
+    rows = np.arange(n)
+    for causal in (False, True):
+        for kl in (None, 0, 17, n):
+            for mask in (None, bm):
+                vis = visible_mask(n, causal, kl, mask, tile)
+                got = bench.row_visible_counts(n, rows, causal, kl, mask, tile=tile)
+                assert np.array_equal(got, vis.sum(axis=1)), (causal, kl, mask is None)
+    # whole workload: lengths per sequence, heads multiply
+    kv = np.array([100, 300], np.int32)
+    assert bench.useful_score_pairs(300, False, kv, None, 2, 3) == 3 * 300 * (100 + 300)
+    assert bench.useful_score_pairs(300, True, None, None, 1, 2) == 2 * 300 * 301 // 2
+
+
+def test_oracle_extrapolation_doubles_the_row_pass():
+    # the column pass is counted at the row pass's cost per visible pair
+    assert bench.extrapolated_oracle_seconds(2.0, 1000, 50000) == pytest.approx(200.0)
+
+
+def test_clock_windows_pick_their_own_samples():
+    s = bench.ClockSampler(0)
+    line = "0, {}, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, {}"
+    s.samples = [(1.0, line.format(2000, "Not Active")), (2.0, line.format(1900, "Active")),
+                 (3.0, line.format(2070, "Not Active")), (4.0, line.format(2070, "Not Active"))]
+    a = s.window(0.5, 2.5)
+    assert a["samples"] == 2 and a["sm_mhz"] == 1950 and a["reasons"] == ["sw_power_cap"]
+    b = s.window(2.5, 5.0)
+    assert b["samples"] == 2 and b["sm_mhz"] == 2070 and b["reasons"] == []
+    assert s.window(10, 11)["samples"] == 0

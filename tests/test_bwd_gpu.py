@@ -76,3 +76,20 @@ def test_bert_large_padded_full_size():
     """Full BERT-large-shaped workload (B16 H16 N512 d64, key padding), every head."""
     inp = inputs.workload_inputs("bert_large_padded")
     check(inp, "bert")
+
+
+@pytest.mark.parametrize("d,N,causal", [(128, 4096, True), (128, 2048, False), (64, 4096, True)])
+def test_long_whole_heads(d, N, causal):
+    """Whole heads with many query tiles per key tile (32 at N = 4096), fwd + bwd
+    element by element; dK, dV also key tile by key tile, so that one tile's error
+    cannot hide in the whole-tensor norm."""
+    inp = inputs.make_inputs(1, 2, N, d, seed=20 + d + N // 1024 + int(causal), causal=causal)
+    got = run_fwd_bwd(inp)
+    ref = oracle_bwd(inp)
+    parity.check_forward(got["o"], got["lse"], ref["o"], ref["lse"], what=f"N={N} d={d}")
+    parity.check_grads(got, ref, what=f"N={N} d={d}")
+    for t in range(N // 128):
+        sl = slice(t * 128, (t + 1) * 128)
+        for name in ("dk", "dv", "dq"):
+            e = parity.rel_fro(got[name][:, :, sl], ref[name][:, :, sl])
+            assert e <= parity.GRAD_REL_FRO, f"N={N} d={d} tile {t} {name} rel-fro {e:.3g}"

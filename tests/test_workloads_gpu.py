@@ -3,10 +3,12 @@ benchmark times (one fa_fwd and one fa_bwd over the whole batch).
 
 Where the fp64 oracle cannot redo the whole workload in seconds it checks what it
 can compute one row or one column at a time:
-  * sampled query rows (O, LSE, dQ) of sampled heads;
-  * for causal masks, every key of the last 128-key tile (dK, dV), whose only
-    queries are the last 128 rows;
-  * whole heads where that is cheap (GPT-2 and block-sparse shapes);
+  * whole heads, element by element (O, LSE, dQ, dK, dV), where one head takes the
+    oracle seconds: GPT-2, block-sparse, and one 16k causal head (whose first key
+    tile accumulates over all 128 query tiles);
+  * at 64k, every query row of the last quarter of one head (O, LSE, dQ) and the dK,
+    dV of three key tiles whose query rows all lie in that quarter (up to 128 query
+    tiles accumulated per key tile), plus sampled rows of other heads;
 and, on every head, identities that hold at any size:
   sum_j dK_j = 0 and sum_j dV_j = sum of dO over rows that see a key.
 """
@@ -76,6 +78,35 @@ def check_last_key_tile(inp, out, head):
         assert e <= parity.GRAD_REL_FRO, f"last key tile {name} rel-fro {e:.3g}"
 
 
+def check_causal_head_block(inp, out, head, row0, key_tiles):
+    """Causal head: O, LSE, dQ of every query row in [row0, N) and dK, dV of the given
+    key tiles (each at or after row0, so every query that sees them is in the block),
+    element by element against the oracle."""
+    b, h = head
+    N = inp.q.shape[2]
+    rows = np.arange(row0, N, dtype=np.int32)
+    r = oracle.head_rows(inp.q[b, h], inp.k[b, h], inp.v[b, h], inp.dout[b, h], inp.scale, causal=True, rows=rows)
+    lse = out["lse"][b, h, row0:].cpu().numpy().astype(np.float64)
+    parity.check_forward(h64(out["o"][b, h, row0:]), lse, r["o"], r["lse"], what=f"head {b},{h} rows {row0}..")
+    e = parity.rel_fro(h64(out["dq"][b, h, row0:]), r["dq"])
+    assert e <= parity.GRAD_REL_FRO, f"head {b},{h} rows {row0}.. dq rel-fro {e:.3g}"
+    m, l, D = (np.full(N, np.nan) for _ in range(3))
+    m[rows], l[rows], D[rows] = r["m"], r["l"], r["D"]
+    cols = np.concatenate([np.arange(t * 128, min(N, t * 128 + 128)) for t in key_tiles]).astype(np.int32)
+    assert cols.min() >= row0
+    c = oracle.head_cols(inp.q[b, h], inp.k[b, h], inp.v[b, h], inp.dout[b, h], inp.scale, m, l, D, causal=True,
+                         cols=cols)
+    idx = torch.from_numpy(cols.astype(np.int64)).cuda()
+    for name in ("dk", "dv"):
+        got = h64(out[name][b, h].index_select(0, idx))
+        e = parity.rel_fro(got, c[name])
+        assert e <= parity.GRAD_REL_FRO, f"head {b},{h} key tiles {key_tiles} {name} rel-fro {e:.3g}"
+        for t in range(len(key_tiles)):  # each tile on its own as well
+            sl = slice(t * 128, (t + 1) * 128)
+            e = parity.rel_fro(got[sl], c[name][sl])
+            assert e <= parity.GRAD_REL_FRO, f"head {b},{h} key tile {key_tiles[t]} {name} rel-fro {e:.3g}"
+
+
 def check_identities(inp, out):
     """sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i (rows that see a key) on every head, in fp64."""
     f64 = torch.float64
@@ -106,6 +137,9 @@ def test_long_causal_16k_full_size():
     inp = inputs.workload_inputs("long_causal_16k")
     out = run_workload(inp)
     N = inp.q.shape[2]
+    # one whole head, element by element, every key tile also on its own: key tile 0
+    # is seen by all 128 query tiles
+    check_causal_head_block(inp, out, (0, 5), 0, list(range(N // 128)))
     rng = np.random.default_rng(0)
     rows = np.unique(np.concatenate([[0, 1, 127, 128, 8191, N - 1], rng.integers(0, N, 40)]))
     check_rows(inp, out, [(0, 0), (0, 13), (0, 31)], rows)
@@ -123,6 +157,8 @@ def test_long_causal_64k_full_size_and_linear_memory():
     rows = np.unique(np.concatenate([[0, 2, 65535, 32768], rng.integers(0, N, 12)]))
     check_rows(inp, out, [(0, 0), (0, 20)], rows)
     check_last_key_tile(inp, out, (0, 9))
+    # the last quarter of one head: key tile 384 accumulates over 128 query tiles
+    check_causal_head_block(inp, out, (0, 9), 3 * N // 4, [384, 448, 511])
     check_identities(inp, out)
     # memory is linear in N: the library allocates nothing, and the caller-side
     # buffers are the [B,H,N,d] tensors plus the O(B*H*N*d) workspace -- far from
