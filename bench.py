@@ -385,6 +385,97 @@ def time_workload(name, steps, warmup, torch, fa, flush, dist=None, override=Non
     return inp, ms, pairs
 
 
+# ---------------------------------------------------- standard attention (comparison)
+
+STANDARD_SWEEP_N = (1024, 2048, 4096, 8192, 16384)
+
+
+def standard_attention(torch, q, k, v, scale, causal):
+    """Standard (materialising) attention, the comparison the method is measured
+    against: the whole score matrix S = scale * Q K^T is written to HBM, then
+    P = softmax(S) (a second N x N tensor), then O = P V -- the three steps of the
+    "Standard Attention" procedure in khetwal.com's worked example and of its section
+    "The Quadratic Memory Bottleneck", written as a framework user writes them
+    (cuBLAS GEMMs and PyTorch's softmax; with autograd, the backward keeps P and
+    forms dP, dS as further N x N tensors).  It shares nothing with the tiled kernels.
+    Inputs [B, H, N, d]; S and P are held in the inputs' dtype."""
+    s = torch.matmul(q, k.transpose(-1, -2))
+    s.mul_(scale)
+    if causal:
+        n = q.shape[-2]
+        above = torch.ones(n, n, dtype=torch.bool, device=q.device).triu_(1)
+        s.masked_fill_(above, float("-inf"))
+    p = torch.softmax(s, dim=-1)
+    return torch.matmul(p, v)
+
+
+def time_standard_vs_tiled(torch, fa, flush, N, B=1, H=32, d=128, causal=True, steps=3, warmup=2, seed=1008):
+    """Device time and peak extra device memory of standard attention and of the tiled
+    path on one causal shape, forward and forward+backward.  Inputs are seeded N(0,1)
+    drawn on the device; the peak is measured above the inputs' own allocation."""
+    gen = torch.Generator(device="cuda").manual_seed(seed + N)
+    shape = (B, H, N, d)
+    q, k, v, do = (torch.randn(shape, generator=gen, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+                   for _ in range(4))
+    scale = 1.0 / math.sqrt(d)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(warmup):
+            flush()
+            fn()
+        torch.cuda.synchronize()
+        ms = 0.0
+        for _ in range(steps):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms += e0.elapsed_time(e1)
+        return ms / steps
+
+    def peak_extra(fn):
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        base = torch.cuda.memory_allocated()
+        torch.cuda.reset_peak_memory_stats()
+        fn()
+        torch.cuda.synchronize()
+        return torch.cuda.max_memory_allocated() - base
+
+    def std_fwd():
+        with torch.no_grad():
+            standard_attention(torch, q, k, v, scale, causal)
+
+    def std_fwd_bwd():
+        qg, kg, vg = (t.detach().requires_grad_(True) for t in (q, k, v))
+        o = standard_attention(torch, qg, kg, vg, scale, causal)
+        o.backward(do)
+
+    def ours_fwd():
+        fa.attention_forward(q, k, v, scale, causal)
+
+    def ours_fwd_bwd():
+        o, lse = fa.attention_forward(q, k, v, scale, causal)
+        fa.attention_backward(q, k, v, o, lse, do, scale, causal)
+
+    row = {"N": N}
+    for name, fn in (("standard_fwd", std_fwd), ("standard_fwd_bwd", std_fwd_bwd), ("tiled_fwd", ours_fwd),
+                     ("tiled_fwd_bwd", ours_fwd_bwd)):
+        row[name + "_ms"] = round(timed(fn), 4)
+        row[name + "_peak_bytes"] = int(peak_extra(fn))
+    if fa.fa_get_device_status() != 0:
+        raise RuntimeError("device status reports a timed-out wait")
+    row["speedup_fwd"] = round(row["standard_fwd_ms"] / row["tiled_fwd_ms"], 2)
+    row["speedup_fwd_bwd"] = round(row["standard_fwd_bwd_ms"] / row["tiled_fwd_bwd_ms"], 2)
+    row["score_matrix_fp32_bytes"] = 4 * B * H * N * N  # the N x N fp32 matrix of the pages' arithmetic
+    del q, k, v, do
+    torch.cuda.empty_cache()
+    return row
+
+
 def leg_report(inp, ms, pairs, peaks, clocks):
     """Throughput, fractions of peak and the roofline of one timed workload."""
     B, H, N, d = inp.q.shape
@@ -760,6 +851,18 @@ def run_ours(args):
                     "clocks": sampler.window(*swin),
                 }
                 del sin
+            if not args.no_standard:
+                std = {"config": {"B": 1, "H": 32, "d": 128, "causal": True, "dtype": "bf16",
+                                  "standard": "cuBLAS GEMMs + PyTorch softmax, S and P materialised in HBM "
+                                              "(bf16); backward by autograd",
+                                  "tiled": "fa_fwd + fa_bwd (this library)",
+                                  "peak": "peak device bytes allocated above the inputs during one call"},
+                       "sweep": []}
+                t0 = time.monotonic()
+                for n in STANDARD_SWEEP_N:
+                    std["sweep"].append(time_standard_vs_tiled(torch, fa, flush, n))
+                std["clocks"] = sampler.window(t0, time.monotonic())
+                line["standard_attention"] = std
     finally:
         sampler.stop()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -821,6 +924,7 @@ def main(argv=None):
     ap.add_argument("--graphs", action="store_true", help="replay one CUDA graph per stage instead of calling the API")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-standard", action="store_true", help="skip the standard-attention comparison sweep")
     ap.add_argument("--cpu-rows", type=int, default=2048, help="query rows the cpu_baseline oracle sample covers")
     ap.add_argument("--ref-rows", type=int, default=1024, help="query rows per reference-arm step")
     args = ap.parse_args(argv)

@@ -135,3 +135,16 @@ def test_clock_windows_pick_their_own_samples():
     b = s.window(2.5, 5.0)
     assert b["samples"] == 2 and b["sm_mhz"] == 2070 and b["reasons"] == []
     assert s.window(10, 11)["samples"] == 0
+
+
+def test_standard_attention_is_the_definition_in_fp64():
+    # the comparison leg's arithmetic, run on the CPU in float64, is the oracle's definition
+    import torch
+    import oracle
+    from io_aware_exact_attention_gb300 import inputs
+    for causal in (False, True):
+        inp = inputs.make_inputs(1, 2, 70, 16, seed=5, causal=causal, with_dout=False)
+        q, k, v = (torch.from_numpy(np.asarray(getattr(inp, n), np.float64)) for n in ("q", "k", "v"))
+        o = bench.standard_attention(torch, q, k, v, inp.scale, causal).numpy()
+        ref_o, _ = oracle.attention_forward(inp.q, inp.k, inp.v, inp.scale, causal=causal)
+        np.testing.assert_allclose(o, ref_o, rtol=1e-11, atol=1e-12)
