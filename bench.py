@@ -805,7 +805,8 @@ def run_ours(args):
             line["e2e"] = {"value": round(3.5 * fwd_formula / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
                            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)}
         del inp
-        if extra:
+        legs = set(args.legs.split(","))
+        if extra and "extras" in legs:
             line["extras"] = {}
             for name in EXTRA_WORKLOADS:
                 if name == args.workload:
@@ -815,6 +816,7 @@ def run_ours(args):
                 xrep = leg_report(xin, xms, xpairs, peaks, sampler.window(*xms["window"]))
                 xrep["roofline"]["traffic"] = recorded_traffic(xrep["roofline"]["kernel"], name)
                 line["extras"][name] = xrep
+        if extra and "fp8" in legs:
             finp, fms, fwin = time_fp8_forward(FP8_WORKLOAD, 10, 3, torch, fa, flush, min_seconds=EXTRA_MIN_SECONDS)
             fB, fH, fN, fd = finp.q8.shape
             ff = formula_fwd_flops(fB, fH, fN, fd, finp.causal)
@@ -832,8 +834,9 @@ def run_ours(args):
                 "clocks": sampler.window(*fwin),
             }
             del finp
+        if extra and "splitkv" in legs:
             line["split_kv"] = {}
-            for qk_name in sorted(inputs.QK_WORKLOADS):
+            for qk_name in sorted(args.splitkv_workloads.split(",")):
                 sin, n_splits, sms, swin = time_splitkv(qk_name, 20, 3, torch, fa, flush,
                                                         min_seconds=EXTRA_MIN_SECONDS)
                 sB, sH, sNq, sd = sin.q.shape
@@ -851,18 +854,18 @@ def run_ours(args):
                     "clocks": sampler.window(*swin),
                 }
                 del sin
-            if not args.no_standard:
-                std = {"config": {"B": 1, "H": 32, "d": 128, "causal": True, "dtype": "bf16",
-                                  "standard": "cuBLAS GEMMs + PyTorch softmax, S and P materialised in HBM "
-                                              "(bf16); backward by autograd",
-                                  "tiled": "fa_fwd + fa_bwd (this library)",
-                                  "peak": "peak device bytes allocated above the inputs during one call"},
-                       "sweep": []}
-                t0 = time.monotonic()
-                for n in STANDARD_SWEEP_N:
-                    std["sweep"].append(time_standard_vs_tiled(torch, fa, flush, n))
-                std["clocks"] = sampler.window(t0, time.monotonic())
-                line["standard_attention"] = std
+        if extra and "standard" in legs and not args.no_standard:
+            std = {"config": {"B": 1, "H": 32, "d": 128, "causal": True, "dtype": "bf16",
+                              "standard": "cuBLAS GEMMs + PyTorch softmax, S and P materialised in HBM "
+                                          "(bf16); backward by autograd",
+                              "tiled": "fa_fwd + fa_bwd (this library)",
+                              "peak": "peak device bytes allocated above the inputs during one call"},
+                   "sweep": []}
+            t0 = time.monotonic()
+            for n in STANDARD_SWEEP_N:
+                std["sweep"].append(time_standard_vs_tiled(torch, fa, flush, n))
+            std["clocks"] = sampler.window(t0, time.monotonic())
+            line["standard_attention"] = std
     finally:
         sampler.stop()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -925,9 +928,16 @@ def main(argv=None):
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-standard", action="store_true", help="skip the standard-attention comparison sweep")
+    ap.add_argument("--legs", default="extras,fp8,splitkv,standard",
+                    help="comma list of the extra legs to run: extras, fp8, splitkv, standard")
+    ap.add_argument("--splitkv-workloads", default=",".join(sorted(inputs.QK_WORKLOADS)),
+                    help="comma list of the split-KV workloads the splitkv leg times")
     ap.add_argument("--cpu-rows", type=int, default=2048, help="query rows the cpu_baseline oracle sample covers")
     ap.add_argument("--ref-rows", type=int, default=1024, help="query rows per reference-arm step")
     args = ap.parse_args(argv)
+    for qk in args.splitkv_workloads.split(","):
+        if qk not in inputs.QK_WORKLOADS:
+            ap.error(f"unknown split-KV workload {qk}")
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.workload == "tiny_fp32":
