@@ -40,22 +40,33 @@ def _inputs():
     return files
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB_PATH):
+# The failure-path test build: waits give up after 5 ms instead of 1 s, and CTA 0 of
+# the d = 128 forward and backward skips one of its tile loads, so that a bounded wait
+# runs out on purpose and the kernel's abort path (drain, TMEM release, status word)
+# runs.  It is a separate library, built only by the tests; libfa_gb300.so never
+# contains it.
+FAULT_TEST_FLAGS = ("-DFA_TEST_SKIP_LOAD", "-DFA_WAIT_LIMIT_NS=5000000ull")
+FAULT_TEST_LIB_PATH = os.path.join(PKG, "libfa_gb300_faulttest.so")
+
+
+def needs_build(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every CUDA source for sm_103a (in parallel) and link libfa_gb300.so."""
-    if not force and not needs_build():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib_path: str = LIB_PATH) -> str:
+    """Compile every CUDA source for sm_103a (in parallel) and link `lib_path`
+    (libfa_gb300.so unless a variant with extra compile flags is asked for)."""
+    if not force and not needs_build(lib_path):
+        return lib_path
+    build_dir = BUILD_DIR if lib_path == LIB_PATH else os.path.join(BUILD_DIR, os.path.basename(lib_path) + ".d")
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         cmd = [nvcc, *NVCC_FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -69,13 +80,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if verbose:
         for obj, log in results:
             print(f"== {os.path.basename(obj)}\n{log}")
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 def _declare(lib):
@@ -111,6 +122,12 @@ def _declare(lib):
     lib.fa_version.argtypes = []
     lib.fa_version.restype = i
     return lib
+
+
+def load_variant(lib_path: str):
+    """A separately built variant of the library (its own handle, its own device status
+    word); see FAULT_TEST_FLAGS."""
+    return _declare(ctypes.CDLL(lib_path))
 
 
 def load():

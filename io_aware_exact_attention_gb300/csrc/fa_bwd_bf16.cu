@@ -176,6 +176,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int h = 0; h < D / 64; ++h)
           tma_load_3d(smQ + sq * L::kTileBytes + h * L::kSubBytes, &tm_q, &bar.q_full[sq], h * 64, qt * kTile, head);
         if (it >= DS && !(ok = mbar_wait(&bar.do_empty[sd], ((it / DS) - 1) & 1, wc))) break;
+#ifdef FA_TEST_SKIP_LOAD
+        // failure-path test build only: CTA 0 never loads its second dO tile, so the MMA
+        // issuer's bounded wait on it gives up and the CTA takes its abort path
+        if (it == 1 && blockIdx.x == 0) continue;
+#endif
         mbar_arrive_expect_tx(&bar.do_full[sd], L::kTileBytes);
         for (int h = 0; h < D / 64; ++h)
           tma_load_3d(smDO + sd * L::kTileBytes + h * L::kSubBytes, &tm_do, &bar.do_full[sd], h * 64, qt * kTile,

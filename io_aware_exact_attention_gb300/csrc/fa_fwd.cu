@@ -288,6 +288,11 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
       for (int kt = next_union(0); kt < TK; kt = next_union(kt + 1), ++u) {
         const int s = u % S;
         if (u >= S && !(ok = mbar_wait(&empty[s], ((u / S) - 1) & 1, wc))) break;
+#ifdef FA_TEST_SKIP_LOAD
+        // failure-path test build only: CTA 0 never loads its second K tile, so the
+        // MMA issuer's bounded wait on it gives up and the CTA takes its abort path
+        if (is_k && u == 1 && blockIdx.x == 0 && !SPLIT) continue;
+#endif
         mbar_arrive_expect_tx(&full[s], L::kTileBytes);
         if (is_k) {
           for (int h = 0; h < L::kTileBytes / L::kSubBytes; ++h)

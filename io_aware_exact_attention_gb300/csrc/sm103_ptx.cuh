@@ -14,8 +14,12 @@ namespace fa {
 // Error codes written to the device status word (match fa_status in fa_gb300.h).
 constexpr unsigned kErrTimeout = 4u;
 
-// Give up on a wait after this many nanoseconds of %globaltimer.
-constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+// Give up on a wait after this many nanoseconds of %globaltimer (1 s).  The failure-
+// path test build compiles with a few milliseconds instead (FA_WAIT_LIMIT_NS).
+#ifndef FA_WAIT_LIMIT_NS
+#define FA_WAIT_LIMIT_NS (1000ull * 1000ull * 1000ull)
+#endif
+constexpr unsigned long long kWaitLimitNs = FA_WAIT_LIMIT_NS;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
