@@ -480,7 +480,7 @@ def leg_report(inp, ms, pairs, peaks, clocks):
     """Throughput, fractions of peak and the roofline of one timed workload."""
     B, H, N, d = inp.q.shape
     causal = inp.causal
-    f = formula_fwd_flops(B, H, N, d, causal)
+    f = formula = formula_fwd_flops(B, H, N, d, causal)
     alg = algorithmic_flops(pairs, d)
     useful = useful_score_pairs(N, causal, inp.kv_len, inp.block_mask, B, H) * 4.0 * d
     bwd_ms = ms["bwd_preprocess"] + ms["bwd_main"] + ms["bwd_postprocess"]
@@ -493,6 +493,14 @@ def leg_report(inp, ms, pairs, peaks, clocks):
     dom = max(kern, key=lambda k2: kern[k2][0])
     achieved = tf(kern[dom][1], kern[dom][0])
     long_step = ms["step"] >= 5.0
+    dense_equivalent = None
+    if inp.block_mask is not None:
+        # a tile mask skips most of the N x N pairs: rates and fractions count the visited
+        # tiles (4*128*128*d per pair forward, 2.5x that backward); the dense formula's
+        # rate is reported beside them as the dense-equivalent figure
+        dense_equivalent = {"fwd_tflops": round(tf(f, ms["fwd"]), 2), "bwd_tflops": round(tf(2.5 * f, bwd_ms), 2),
+                            "fwd_bwd_tflops": round(tf(3.5 * f, ms["step"]), 2)}
+        f = alg["fwd"]
     rep = {
         "config": {"B": B, "H": H, "N": N, "d": d, "causal": causal, "key_padding": inp.kv_len is not None,
                    "block_mask": inp.block_mask is not None, "seed": inp.seed},
@@ -509,7 +517,7 @@ def leg_report(inp, ms, pairs, peaks, clocks):
                           "fwd_bwd": round(tf(3.5 * useful, ms["step"]), 2)},
         "stage_ms": {k2: round(v2, 5) for k2, v2 in ms.items() if k2 not in ("wall_s", "launch", "steps", "window")},
         "timed_steps": ms["steps"],
-        "flops_per_step": {"formula_fwd": f, "formula_fwd_bwd": 3.5 * f, "visited_tile_pairs": pairs,
+        "flops_per_step": {"formula_fwd": formula, "formula_fwd_bwd": 3.5 * formula, "visited_tile_pairs": pairs,
                            "algorithmic_fwd": alg["fwd"], "algorithmic_bwd": alg["bwd"],
                            "useful_fwd": useful, "useful_fwd_bwd": 3.5 * useful},
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 2), "peak": burst,
@@ -517,6 +525,9 @@ def leg_report(inp, ms, pairs, peaks, clocks):
                      "peak_source": f"bf16_tflops burst, {peaks['source']}"},
         "clocks": clocks,
     }
+    if dense_equivalent is not None:
+        rep["flops_basis"] = "visited 128x128 tile pairs (block mask)"
+        rep["dense_equivalent"] = dense_equivalent
     if long_step:
         sus = peaks["bf16_tflops_sustained"]
         rep["roofline"]["frac_of_sustained"] = round(achieved / sus, 4)

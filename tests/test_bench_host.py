@@ -148,3 +148,18 @@ def test_standard_attention_is_the_definition_in_fp64():
         o = bench.standard_attention(torch, q, k, v, inp.scale, causal).numpy()
         ref_o, _ = oracle.attention_forward(inp.q, inp.k, inp.v, inp.scale, causal=causal)
         np.testing.assert_allclose(o, ref_o, rtol=1e-11, atol=1e-12)
+
+
+def test_block_mask_legs_count_visited_tiles():
+    from io_aware_exact_attention_gb300 import inputs
+    inp = inputs.make_inputs(1, 2, 512, 64, seed=3, block_mask=dict(band=0, global_cols=0, frac=0.0))
+    pairs = bench.visited_tile_pairs(512, False, None, inp.block_mask, 1, 2)
+    assert pairs == 2 * 4  # the diagonal tiles only
+    ms = {"fwd": 1.0, "bwd_preprocess": 0.1, "bwd_main": 2.0, "bwd_postprocess": 0.1, "stages_sum": 3.2,
+          "step": 3.2, "wall_s": 1.0, "launch": "api calls", "steps": 10, "window": (0.0, 1.0)}
+    peaks = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "test"}
+    rep = bench.leg_report(inp, ms, pairs, peaks, bench.parse_clock_lines([]))
+    alg = bench.algorithmic_flops(pairs, 64)
+    assert rep["fwd_tflops"] == round(alg["fwd"] / 1e-3 / 1e12, 2)
+    assert rep["dense_equivalent"]["fwd_tflops"] == round(bench.formula_fwd_flops(1, 2, 512, 64, False) / 1e-3 / 1e12, 2)
+    assert rep["flops_per_step"]["formula_fwd"] == bench.formula_fwd_flops(1, 2, 512, 64, False)
