@@ -85,7 +85,8 @@ struct FwdBarriers {
   uint64_t k_empty[S];  // both score products have read the K tile of the stage
   uint64_t v_empty[S];  // both P V products have read the V tile of the stage
   uint64_t s_full[2];
-  uint64_t p_full[2];
+  uint64_t p_full[2];  // P of the tile is in TMEM and O rescaled if it had to be (FP8: keys [0, 64) of P)
+  uint64_t p_hi[2];    // FP8 only: P of keys [64, 128) is in TMEM
   uint64_t o_done[2];
   uint64_t drain[2];  // one per MMA issuer
   uint64_t tok[2];    // tok[i]: issuer i has issued its batch (the other issuer's turn)
@@ -151,6 +152,29 @@ __device__ __forceinline__ float row_sum128(const float (&v)[kTile]) {
   for (int c = 8; c < kTile; c += 8)
 #pragma unroll
     for (int k = 0; k < 8; k += 2) fadd2(a[k], a[k + 1], v[c + k], v[c + k + 1]);
+  return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+}
+
+// Registers -> TMEM, 32 lanes x 16 columns in one store and one wait.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// Sum of 64 values v[c0 .. c0+63]: eight independent accumulators (paired adds).
+__device__ __forceinline__ float half_sum64(const float (&v)[kTile], int c0) {
+  float a[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a[k] = v[c0 + k];
+#pragma unroll
+  for (int c = 8; c < 64; c += 8)
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) fadd2(a[k], a[k + 1], v[c0 + c + k], v[c0 + c + k + 1]);
   return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
 }
 
@@ -248,6 +272,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.s_full[i], 1);
       mbar_init(&bar.p_full[i], 128);
+      mbar_init(&bar.p_hi[i], 128);
       mbar_init(&bar.o_done[i], 1);
       mbar_init(&bar.drain[i], 1);
       mbar_init(&bar.tok[i], 1);
@@ -399,11 +424,18 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
           tc_fence_after();
           const uint32_t vs = v0 + s * L::kTileBytes;
           if constexpr (F8) {
-            // V^T K-major: 32 keys = 32 bytes per step; P: four keys per TMEM column
+            // V^T K-major: 32 keys = 32 bytes per step; P: four keys per TMEM column.  P V on
+            // keys [0, 64) while the softmax warps finish keys [64, 128), then the rest.
 #pragma unroll
-            for (int k = 0; k < kTile / 32; ++k)
+            for (int k = 0; k < kTile / 32; ++k) {
+              if (k == kTile / 64) {
+                if (!(ok = mbar_wait(&bar.p_hi[i], n & 1, wc))) break;
+                tc_fence_after();
+              }
               mma_f8_ts(tmem + L::col_o(i), tmem + L::col_s(i) + k * 8, sdesc_sw128(vs + k * 32, 16, 1024), idesc_o,
                         (n > 0 || k > 0) ? 1u : 0u);
+            }
+            if (!ok) break;
           } else {
             // V N-major: 16 keys = 2048 bytes per step; P: two keys per TMEM column
 #pragma unroll
@@ -473,25 +505,28 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
         const float m_new = (mx > m_run + kRescaleSlack) ? mx : m_run;
         const float m_use = (m_new == neg_inf()) ? 0.f : m_new;
         const float alpha = ex2(m_run - m_use);
-        // all exponentials first (independent, so they overlap), then sums and packing;
-        // scale-and-subtract and the sums run two lanes per instruction
+        // P replaces S in the tile's TMEM buffer.  All exponentials of a batch first
+        // (independent, so they overlap), then sums and packing; scale-and-subtract and
+        // the sums run two lanes per instruction.  bf16: one batch of 128 keys, P as bf16
+        // pairs in columns [0, 64).  FP8: two batches of 64 keys, P as E4M3 quads in
+        // columns [0, 16) then [16, 32), so that the MMA warp starts P V on keys [0, 64)
+        // while the exponentials and the (costlier) E4M3 packing of [64, 128) run.
+        constexpr int kFirst = F8 ? kTile / 2 : kTile;
 #pragma unroll
-        for (int c = 0; c < kTile; c += 2) {
+        for (int c = 0; c < kFirst; c += 2) {
           ffma2(s[c], s[c + 1], s[c], s[c + 1], sl2, -m_use);
           s[c] = ex2(s[c]);
           s[c + 1] = ex2(s[c + 1]);
         }
-        const float tile_sum = row_sum128(s);
-        l_run = l_run * alpha + tile_sum;
-        m_run = m_new;
+        float tile_sum;
         if constexpr (F8) {
-          // P replaces S in the tile's TMEM buffer (E4M3 quads, columns [0, 32))
-          uint32_t pk[kTile / 4];
+          tile_sum = half_sum64(s, 0);
+          uint32_t pk[kTile / 8];
 #pragma unroll
-          for (int c = 0; c < kTile; c += 4) pk[c / 4] = pack_e4m3x4(s[c], s[c + 1], s[c + 2], s[c + 3]);
-          tmem_st32(t_s, pk);
+          for (int c = 0; c < kTile / 2; c += 4) pk[c / 4] = pack_e4m3x4(s[c], s[c + 1], s[c + 2], s[c + 3]);
+          tmem_st16(t_s, pk);
         } else {
-          // P replaces S in the tile's TMEM buffer (bf16 pairs, columns [0, 64))
+          tile_sum = row_sum128(s);
           uint32_t pk[kTile / 2];
 #pragma unroll
           for (int c = 0; c < kTile; c += 2) pk[c / 2] = pack_bf16x2(s[c], s[c + 1]);
@@ -514,6 +549,24 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
         }
         tc_fence_before();
         mbar_arrive(&bar.p_full[wg]);
+        if constexpr (F8) {
+#pragma unroll
+          for (int c = kTile / 2; c < kTile; c += 2) {
+            ffma2(s[c], s[c + 1], s[c], s[c + 1], sl2, -m_use);
+            s[c] = ex2(s[c]);
+            s[c + 1] = ex2(s[c + 1]);
+          }
+          uint32_t pk[kTile / 8];
+#pragma unroll
+          for (int c = kTile / 2; c < kTile; c += 4)
+            pk[(c - kTile / 2) / 4] = pack_e4m3x4(s[c], s[c + 1], s[c + 2], s[c + 3]);
+          tmem_st16(t_s + kTile / 8, pk);
+          tc_fence_before();
+          mbar_arrive(&bar.p_hi[wg]);
+          tile_sum += half_sum64(s, kTile / 2);
+        }
+        l_run = l_run * alpha + tile_sum;
+        m_run = m_new;
       }
 
       // epilogue: O = O_acc / l (bf16, staged in this tile's Q buffer, stored by TMA); LSE = m + ln l
