@@ -54,9 +54,9 @@ def test_host_side_errors_launch_nothing():
 
 @pytest.fixture(scope="module")
 def fault_lib():
-    """The failure-path test build (5 ms wait limit; CTA 0 of the d = 128 forward and
-    backward skips one tile load), loaded beside the normal library.  Built here, on
-    first use; the normal build does not contain it."""
+    """The failure-path test build (5 ms wait limit; CTA 0 of the d = 128 bf16 and FP8
+    forward and of the d = 128 backward skips one tile load), loaded beside the normal
+    library.  Built here, on first use; the normal build does not contain it."""
     path = _lib.build(extra_flags=_lib.FAULT_TEST_FLAGS, lib_path=_lib.FAULT_TEST_LIB_PATH)
     return _lib.load_variant(path)
 
@@ -112,3 +112,24 @@ def test_backward_wait_timeout_drains_and_reports(fault_lib):
     ref = oracle.attention_backward(inp.q, inp.k, inp.v, inp.dout, inp.scale, causal=True)
     h = parity.to_host64
     parity.check_grads({"dq": h(dq2), "dk": h(dk2), "dv": h(dv2)}, ref, what="backward after an aborted call")
+
+
+def test_fp8_forward_wait_timeout_drains_and_reports(fault_lib):
+    # the FP8 forward shares the producer hook: CTA 0's issuers give up on the K tile
+    # that never arrives, drain and release TMEM; the normal FP8 forward afterwards is
+    # held to the FP8 error model
+    from tests import test_fp8_gpu as F
+    inp = inputs.make_fp8_inputs(1, 2, 512, 128, seed=83, causal=True)
+    dev, _, _ = F.to_dev(inp)
+    o = torch.empty((1, 2, 512, 128), device="cuda", dtype=torch.bfloat16)
+    lse = torch.empty((1, 2, 512), device="cuda", dtype=torch.float32)
+    stream = torch.cuda.current_stream().cuda_stream
+    assert fault_lib.fa_get_device_status(stream) == _lib.FA_OK
+    ldv = int(dev["vt8"].stride(2))
+    rc = fault_lib.fa_fwd_fp8(_ptr(dev["q8"]), _ptr(dev["k8"]), _ptr(dev["vt8"]), ldv, _ptr(o), _ptr(lse), 1, 2, 512,
+                              128, inp.scale, inp.descale_q, inp.descale_k, inp.descale_v, 1, None, None, stream)
+    assert rc == _lib.FA_OK
+    assert fault_lib.fa_get_device_status(stream) == _lib.FA_ERR_TIMEOUT
+    assert fault_lib.fa_get_device_status(stream) == _lib.FA_OK
+    o2, lse2 = F.run(inp)
+    F.check_all(inp, o2, lse2)
