@@ -43,6 +43,8 @@ namespace {
 
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleSlack = 8.0f;  // P values stay below 2^8 before a rescale is forced
+// bf16: a key tile whose exponentials against the running max sum to at most 2^8 keeps it
+constexpr float kFastSumLimit = 256.0f;  // = 2^kRescaleSlack
 
 // NQ query tiles per CTA.  NQ = 2 (d = 128): one CTA per SM, the two tiles'
 // softmax phases overlap each other's MMAs.  NQ = 1 (d = 64): a lighter CTA with
@@ -485,26 +487,36 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
         ok = mbar_wait(&bar.s_full[wg], n & 1, wc);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
+        // S of this key tile into registers, masked: key padding tail, causal diagonal
+        // (the N tail is covered by kv_len <= N)
         float s[kTile];
-#pragma unroll
-        for (int c0 = 0; c0 < kTile; c0 += 64) {
-          uint32_t t[64];
-          tmem_ld64(t_s + c0, t);
-#pragma unroll
-          for (int i = 0; i < 64; ++i) s[c0 + i] = __uint_as_float(t[i]);
-        }
-        // element mask: key padding tail, causal diagonal (the N tail is covered by kv_len <= N)
         const int key0 = kt * kTile;
-        if (key0 + kTile > kv_len || (a.causal && kt == my_qt)) {
-          const int lim = a.causal ? min(kv_len, q_row + 1) : kv_len;  // keys [key0, lim) visible
+        const bool edge = key0 + kTile > kv_len || (a.causal && kt == my_qt);
+        auto load_scores = [&]() {
 #pragma unroll
-          for (int c = 0; c < kTile; ++c)
-            if (key0 + c >= lim) s[c] = neg_inf();
-        }
-        const float mx = row_max128(s) * sl2;
-        const float m_new = (mx > m_run + kRescaleSlack) ? mx : m_run;
-        const float m_use = (m_new == neg_inf()) ? 0.f : m_new;
-        const float alpha = ex2(m_run - m_use);
+          for (int c0 = 0; c0 < kTile; c0 += 64) {
+            uint32_t t[64];
+            tmem_ld64(t_s + c0, t);
+#pragma unroll
+            for (int i = 0; i < 64; ++i) s[c0 + i] = __uint_as_float(t[i]);
+          }
+          if (edge) {
+            const int lim = a.causal ? min(kv_len, q_row + 1) : kv_len;  // keys [key0, lim) visible
+#pragma unroll
+            for (int c = 0; c < kTile; ++c)
+              if (key0 + c >= lim) s[c] = neg_inf();
+          }
+        };
+        load_scores();
+        // The stabiliser m_use of the exponentials.  bf16, after the first key tile: the
+        // exponentials are formed against the running max first, and kept when they sum to
+        // at most 2^8.  P >= 0, so then every term is at most 2^8: the tile's max lies
+        // within kRescaleSlack of the running max, where the max rule below keeps the
+        // running max too, and the values are exactly the ones that rule would form.  A
+        // larger (or NaN or infinite) sum falls back to the rule, with S reloaded from TMEM.
+        // This skips the row max, a sixth of the softmax's instructions, whenever the max
+        // does not move.  The first tile and FP8 (P formed in halves) always take the rule.
+        //
         // P replaces S in the tile's TMEM buffer.  All exponentials of a batch first
         // (independent, so they overlap), then sums and packing; scale-and-subtract and
         // the sums run two lanes per instruction.  bf16: one batch of 128 keys, P as bf16
@@ -512,13 +524,28 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
         // columns [0, 16) then [16, 32), so that the MMA warp starts P V on keys [0, 64)
         // while the exponentials and the (costlier) E4M3 packing of [64, 128) run.
         constexpr int kFirst = F8 ? kTile / 2 : kTile;
+        float m_new = m_run, m_use = m_run, alpha = 1.f, tile_sum = 0.f;
+        bool with_max = F8 || n == 0;
+#pragma unroll 1
+        for (int pass = 0;; ++pass) {
+          if (with_max) {
+            if (pass > 0) load_scores();
+            const float mx = row_max128(s) * sl2;
+            m_new = (mx > m_run + kRescaleSlack) ? mx : m_run;
+            m_use = (m_new == neg_inf()) ? 0.f : m_new;
+            alpha = ex2(m_run - m_use);
+          }
 #pragma unroll
-        for (int c = 0; c < kFirst; c += 2) {
-          ffma2(s[c], s[c + 1], s[c], s[c + 1], sl2, -m_use);
-          s[c] = ex2(s[c]);
-          s[c + 1] = ex2(s[c + 1]);
+          for (int c = 0; c < kFirst; c += 2) {
+            ffma2(s[c], s[c + 1], s[c], s[c + 1], sl2, -m_use);
+            s[c] = ex2(s[c]);
+            s[c + 1] = ex2(s[c + 1]);
+          }
+          if constexpr (F8) break;
+          tile_sum = row_sum128(s);
+          if (with_max || !__any_sync(0xffffffffu, !(tile_sum <= kFastSumLimit))) break;
+          with_max = true;
         }
-        float tile_sum;
         if constexpr (F8) {
           tile_sum = half_sum64(s, 0);
           uint32_t pk[kTile / 8];
@@ -526,7 +553,6 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
           for (int c = 0; c < kTile / 2; c += 4) pk[c / 4] = pack_e4m3x4(s[c], s[c + 1], s[c + 2], s[c + 3]);
           tmem_st16(t_s, pk);
         } else {
-          tile_sum = row_sum128(s);
           uint32_t pk[kTile / 2];
 #pragma unroll
           for (int c = 0; c < kTile; c += 2) pk[c / 2] = pack_bf16x2(s[c], s[c + 1]);

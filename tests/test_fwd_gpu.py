@@ -1,4 +1,6 @@
 """Forward parity: the CUDA path (through the C ABI) against the fp64 oracle."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -39,6 +41,29 @@ def test_bf16_ragged_sizes(N, d, causal):
     o, lse = run_fwd(inp)
     ro, rl = oracle_fwd(inp)
     parity.check_forward(o, lse, ro, rl, what=f"N={N} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_running_max_jumps_between_key_tiles(d, causal):
+    # Scores of even query rows jump between key tiles by a planted component (natural
+    # log units 0, +5, +20, +28, -2 for key tiles 0..4), so the d = 128 kernel's three
+    # per-tile paths all occur: exponentials against the running max kept (their sum at
+    # most 2^8), the row max taken but the running max kept (within the rescale slack),
+    # and the running max raised with an O rescale (+20, +28).  Odd rows keep plain
+    # N(0,1)-scaled scores, so warps mix the cases.
+    N = 640
+    inp = inputs.make_inputs(1, 2, N, d, seed=901 + d + int(causal), causal=causal, with_dout=False)
+    jump = np.array([0.0, 5.0, 20.0, 28.0, -2.0], np.float32)
+    a = 8.0
+    q, k = inp.q.copy(), inp.k.copy()
+    q[:, :, 0::2, 0] = a
+    q[:, :, 1::2, 0] = 0.0
+    k[:, :, :, 0] = inputs.round_bf16(np.repeat(jump, 128)[None, None, :] * np.sqrt(d) / a)
+    inp = dataclasses.replace(inp, q=q, k=k)
+    o, lse = run_fwd(inp)
+    ro, rl = oracle_fwd(inp)
+    parity.check_forward(o, lse, ro, rl, what=f"max jumps d={d} causal={causal}")
 
 
 @pytest.mark.parametrize("d", [64, 128])
