@@ -66,6 +66,22 @@ struct BwdLayout {
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
+// The eight K = 16 steps of a 128-deep product over 128-byte-swizzled bf16 tiles, in
+// descriptor units (16 bytes): a K-major operand moves 32 bytes inside a 64-element
+// sub-tile, then to the next sub-tile (kSubBytes on); an M- or N-major operand moves 16
+// rows of 128 bytes (2048 bytes).  kk: both K-major (S, dP); mn: both M/N-major (dV,
+// dK); kn: A K-major, B N-major (dQ).
+static_assert(BwdLayout<128>::kSubBytes == 1024 * 16, "K-major step offsets below");
+__device__ __forceinline__ void mma_steps_kk(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  mma8_bf16_ss<0, 2, 4, 6, 1024, 1026, 1028, 1030, 0, 2, 4, 6, 1024, 1026, 1028, 1030>(d, a, b, idesc, acc);
+}
+__device__ __forceinline__ void mma_steps_mn(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  mma8_bf16_ss<0, 128, 256, 384, 512, 640, 768, 896, 0, 128, 256, 384, 512, 640, 768, 896>(d, a, b, idesc, acc);
+}
+__device__ __forceinline__ void mma_steps_kn(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  mma8_bf16_ss<0, 2, 4, 6, 1024, 1026, 1028, 1030, 0, 128, 256, 384, 512, 640, 768, 896>(d, a, b, idesc, acc);
+}
+
 template <int D>
 struct BwdBarriers {
   uint64_t kv_full;
@@ -210,11 +226,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto issue_scores = [&](int stage) {
         const uint64_t qd = sdesc_sw128(smem_u32(smQ + stage * L::kTileBytes), 16, 1024);
         tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
-          mma_bf16_ss(tmem + L::kColSP, sdesc_adv(qd, off), sdesc_adv(kd, off), id_s, k > 0 ? 1u : 0u);
-        }
+        mma_steps_kk(tmem + L::kColSP, qd, kd, id_s, 0u);
         mma_commit(&bar.s_full);
       };
       if (first < T) {
@@ -234,19 +246,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!(ok = mbar_wait(&bar.do_full[sd], (it / DS) & 1, wc))) break;
           if (!(ok = mbar_wait(&bar.s_free, it & 1, wc))) break;
           tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
-            mma_bf16_ss(tmem + L::kColSP, sdesc_adv(dod, off), sdesc_adv(vd, off), id_s, k > 0 ? 1u : 0u);
-          }
+          mma_steps_kk(tmem + L::kColSP, dod, vd, id_s, 0u);
           mma_commit(&bar.dp_full);
           // dV += P^T dO_i
           if (!(ok = mbar_wait(&bar.p_full, it & 1, wc))) break;
           tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < kTile / 16; ++k)
-            mma_bf16_ss(tmem + L::kColDV, sdesc_adv(pt, k * 2048), sdesc_adv(don, k * 2048), id_t,
-                        (it > 0 || k > 0) ? 1u : 0u);
+          mma_steps_mn(tmem + L::kColDV, pt, don, id_t, it > 0 ? 1u : 0u);
           mma_commit(&bar.dv_done);
           mma_commit(&bar.do_empty[sd]);
           // the next scores
@@ -258,18 +263,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // dK += dS^T Q_i (the last reader of Q_i)
           if (!(ok = mbar_wait(&bar.ds_full, it & 1, wc))) break;
           tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < kTile / 16; ++k)
-            mma_bf16_ss(tmem + L::kColDK, sdesc_adv(pt, k * 2048), sdesc_adv(qn, k * 2048), id_t,
-                        (it > 0 || k > 0) ? 1u : 0u);
+          mma_steps_mn(tmem + L::kColDK, pt, qn, id_t, it > 0 ? 1u : 0u);
           mma_commit(&bar.q_empty[sq]);
           // dQ_i = dS K_j
           if (it >= 1 && !(ok = mbar_wait(&bar.dq_free, (it - 1) & 1, wc))) break;
           tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < kTile / 16; ++k)
-            mma_bf16_ss(tmem + L::kColDQ, sdesc_adv(pk, (k / 4) * L::kSubBytes + (k % 4) * 32),
-                        sdesc_adv(kn, k * 2048), id_q, k > 0 ? 1u : 0u);
+          mma_steps_kn(tmem + L::kColDQ, pk, kn, id_q, 0u);
           mma_commit(&bar.dkdq_done);  // dS is no longer read, dQ_i is complete
           qt = qt_next;
         }
@@ -355,14 +354,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       mbar_arrive(&bar.p_full);
 
-      // dS = P * (dP - D), one 64-column half at a time.  dS replaces P in the shared
-      // buffer once the dV MMA has read P (waited before the first half is written);
-      // the MMA warp may write the next S over dP once the second half is loaded (the
-      // pipe is still busy with dV until about then).
+      // dS = P * (dP - D), one 64-column half at a time, P read back from the rows of the
+      // shared buffer this thread wrote.  dS replaces P there once the dV MMA has read P
+      // (waited before the first half is written); the MMA warp may write the next S over
+      // dP once the second half is loaded (the pipe is still busy with dV until about
+      // then).  The halves run through one loop body: with P in registers both halves
+      // were separate code, and this kernel's roles together outgrew the instruction
+      // cache (64% hits); one body, and one for the dQ drain below, took 9% off its time.
       ok = mbar_wait(&bar.dp_full, it & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll
+#pragma unroll 1
       for (int c0 = 0; c0 < kTile; c0 += 64) {
         uint32_t t[64];
         tmem_ld64(tmem + lane_off + L::kColSP + c0, t);
@@ -370,12 +372,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_before();
           mbar_arrive(&bar.dp_free);
         }
+        uint32_t pp[32];
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          ld_shared_v4(psrow + (c0 / 64) * L::kSubBytes + sw128_offset(r, g), pp[4 * g], pp[4 * g + 1], pp[4 * g + 2],
+                       pp[4 * g + 3]);
         float f[64];
 #pragma unroll
-        for (int i = 0; i < 64; i += 2) {
-          const uint32_t pp = pk[(c0 + i) / 2];
-          fsubmul2(f[i], f[i + 1], __uint_as_float(t[i]), __uint_as_float(t[i + 1]), d_r, bf16lo(pp), bf16hi(pp));
-        }
+        for (int i = 0; i < 64; i += 2)
+          fsubmul2(f[i], f[i + 1], __uint_as_float(t[i]), __uint_as_float(t[i + 1]), d_r, bf16lo(pp[i / 2]),
+                   bf16hi(pp[i / 2]));
         uint32_t w[32];
 #pragma unroll
         for (int i = 0; i < 64; i += 2) w[i / 2] = pack_bf16x2(f[i], f[i + 1]);
@@ -411,7 +417,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = mbar_wait(&bar.dkdq_done, it & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll
+#pragma unroll 1
       for (int c64 = 0; c64 < D; c64 += 64) {
         uint32_t t[64];
         tmem_ld64(tmem + lane_off + L::kColDQ + c64, t);

@@ -254,6 +254,31 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// Eight kind::f16 MMAs from shared memory into one accumulator, one K = 16 step each:
+// descriptor k of A (B) is `a` (`b`) plus the compile-time offset Ak (Bk), in the
+// descriptor's 16-byte units.  The first MMA accumulates when `acc` is non-zero, the
+// other seven always.  One asm block: the predicates are set once and each step is two
+// adds and the MMA, which keeps the single issuing thread ahead of the tensor pipe.
+template <uint32_t A0, uint32_t A1, uint32_t A2, uint32_t A3, uint32_t A4, uint32_t A5, uint32_t A6, uint32_t A7,
+          uint32_t B0, uint32_t B1, uint32_t B2, uint32_t B3, uint32_t B4, uint32_t B5, uint32_t B6, uint32_t B7>
+__device__ __forceinline__ void mma8_bf16_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
+      "add.s64 da, %1, %6;\n\tadd.s64 db, %2, %14;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p0;\n\t"
+      "add.s64 da, %1, %7;\n\tadd.s64 db, %2, %15;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p1;\n\t"
+      "add.s64 da, %1, %8;\n\tadd.s64 db, %2, %16;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p1;\n\t"
+      "add.s64 da, %1, %9;\n\tadd.s64 db, %2, %17;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p1;\n\t"
+      "add.s64 da, %1, %10;\n\tadd.s64 db, %2, %18;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p1;\n\t"
+      "add.s64 da, %1, %11;\n\tadd.s64 db, %2, %19;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p1;\n\t"
+      "add.s64 da, %1, %12;\n\tadd.s64 db, %2, %20;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p1;\n\t"
+      "add.s64 da, %1, %13;\n\tadd.s64 db, %2, %21;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p1;\n\t}\n"
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(1u),
+      "n"(A0), "n"(A1), "n"(A2), "n"(A3), "n"(A4), "n"(A5), "n"(A6), "n"(A7),
+      "n"(B0), "n"(B1), "n"(B2), "n"(B3), "n"(B4), "n"(B5), "n"(B6), "n"(B7)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -382,6 +407,11 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float x0, float x1, float x2, fl
 
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// 16 bytes from shared memory (the counterpart of st_shared_v4).
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
+}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
