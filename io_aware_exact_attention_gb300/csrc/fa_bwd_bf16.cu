@@ -313,13 +313,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool need_mask = (key0 + kTile > kv_len) || (a.causal && kt == qt);
       const int lim = a.causal ? min(kv_len, q_row + 1) : kv_len;  // keys [key0, lim) visible
 
-      // P = exp2(S scale log2e - LSE log2e), one 64-column half at a time; the MMA warp
-      // may write dP over S once both halves are in registers
+      // P = exp2(S scale log2e - LSE log2e), one 64-column half at a time through one loop
+      // body (see the dS loop below); the MMA warp may write dP over S once both halves are
+      // in registers.  The first half's bf16 pairs are held while the second is formed,
+      // then both are stored once the previous dS is no longer read.
       ok = mbar_wait(&bar.s_full, it & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      uint32_t pk[kTile / 2];
-#pragma unroll
+      uint32_t pk0[32];
+#pragma unroll 1
       for (int c0 = 0; c0 < kTile; c0 += 64) {
         uint32_t t[64];
         tmem_ld64(tmem + lane_off + L::kColSP + c0, t);
@@ -339,17 +341,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int i = 0; i < 64; ++i)
             if (key0 + c0 + i >= lim) f[i] = 0.f;
         }
+        uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 64; i += 2) pk[(c0 + i) / 2] = pack_bf16x2(f[i], f[i + 1]);
-      }
-      if (it >= 1) {
-        ok = mbar_wait(&bar.dkdq_done, (it - 1) & 1, wc);  // dS_{i-1} no longer read by the dK, dQ MMAs
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      }
+        for (int i = 0; i < 64; i += 2) pk[i / 2] = pack_bf16x2(f[i], f[i + 1]);
+        if (c0 == 0) {
 #pragma unroll
-      for (int g = 0; g < kTile / 8; ++g)
-        st_shared_v4(psrow + (g / 8) * L::kSubBytes + sw128_offset(r, g % 8), pk[4 * g], pk[4 * g + 1],
-                     pk[4 * g + 2], pk[4 * g + 3]);
+          for (int j = 0; j < 32; ++j) pk0[j] = pk[j];
+        } else {
+          if (it >= 1) {
+            ok = mbar_wait(&bar.dkdq_done, (it - 1) & 1, wc);  // dS_{i-1} no longer read by the dK, dQ MMAs
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          }
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            st_shared_v4(psrow + sw128_offset(r, g), pk0[4 * g], pk0[4 * g + 1], pk0[4 * g + 2], pk0[4 * g + 3]);
+            st_shared_v4(psrow + L::kSubBytes + sw128_offset(r, g), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2],
+                         pk[4 * g + 3]);
+          }
+        }
+      }
+      if (!ok) break;
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bar.p_full);

@@ -384,15 +384,22 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
       auto issue_scores = [&](int stage) {
         tc_fence_after();
         const uint32_t ks = k0 + stage * L::kTileBytes;
+        if constexpr (!F8 && D == 128) {
+          // eight K = 16 steps: 32 bytes inside a 64-element sub-tile, then the next sub-tile
+          static_assert(L::kSubBytes == 1024 * 16, "step offsets in 16-byte units");
+          mma8_bf16_ss<0, 2, 4, 6, 1024, 1026, 1028, 1030, 0, 2, 4, 6, 1024, 1026, 1028, 1030>(
+              tmem + L::col_s(i), sdesc_sw128(qs, 16, 1024), sdesc_sw128(ks, 16, 1024), idesc_s, 0u);
+        } else {
 #pragma unroll
-        for (int k = 0; k < D * L::kElem / 32; ++k) {  // 32 bytes of each row per MMA
-          const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
-          if constexpr (F8)
-            mma_f8_ss(tmem + L::col_s(i), sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + off, 16, 1024), idesc_s,
-                      k > 0 ? 1u : 0u);
-          else
-            mma_bf16_ss(tmem + L::col_s(i), sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + off, 16, 1024),
+          for (int k = 0; k < D * L::kElem / 32; ++k) {  // 32 bytes of each row per MMA
+            const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
+            if constexpr (F8)
+              mma_f8_ss(tmem + L::col_s(i), sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + off, 16, 1024),
                         idesc_s, k > 0 ? 1u : 0u);
+            else
+              mma_bf16_ss(tmem + L::col_s(i), sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + off, 16, 1024),
+                          idesc_s, k > 0 ? 1u : 0u);
+          }
         }
       };
       int kt = union_from(0);
@@ -439,11 +446,10 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
             }
             if (!ok) break;
           } else {
-            // V N-major: 16 keys = 2048 bytes per step; P: two keys per TMEM column
-#pragma unroll
-            for (int k = 0; k < kTile / 16; ++k)
-              mma_bf16_ts(tmem + L::col_o(i), tmem + L::col_s(i) + k * 8,
-                          sdesc_sw128(vs + k * 2048, L::kSubBytes, 1024), idesc_o, (n > 0 || k > 0) ? 1u : 0u);
+            // V N-major: 16 keys = 2048 bytes per step; P: two keys (eight per K step) per TMEM column
+            mma8_bf16_ts<0, 128, 256, 384, 512, 640, 768, 896>(tmem + L::col_o(i), tmem + L::col_s(i),
+                                                                sdesc_sw128(vs, L::kSubBytes, 1024), idesc_o,
+                                                                n > 0 ? 1u : 0u);
           }
         }
         if (fn) {

@@ -279,6 +279,28 @@ __device__ __forceinline__ void mma8_bf16_ss(uint32_t d_tmem, uint64_t a, uint64
       : "memory");
 }
 
+// The same with A from tensor memory (the TS form): step k reads A at a_tmem + 8k
+// (two bf16 K-elements per 32-bit column, so K = 16 is eight columns) and B at b plus
+// the k-th offset.
+template <uint32_t B0, uint32_t B1, uint32_t B2, uint32_t B3, uint32_t B4, uint32_t B5, uint32_t B6, uint32_t B7>
+__device__ __forceinline__ void mma8_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 db;\n\t.reg .b32 ta;\n\t"
+      "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
+      "add.s64 db, %2, %6;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p0;\n\t"
+      "add.u32 ta, %1, 8;\n\tadd.s64 db, %2, %7;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p1;\n\t"
+      "add.u32 ta, %1, 16;\n\tadd.s64 db, %2, %8;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p1;\n\t"
+      "add.u32 ta, %1, 24;\n\tadd.s64 db, %2, %9;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p1;\n\t"
+      "add.u32 ta, %1, 32;\n\tadd.s64 db, %2, %10;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p1;\n\t"
+      "add.u32 ta, %1, 40;\n\tadd.s64 db, %2, %11;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p1;\n\t"
+      "add.u32 ta, %1, 48;\n\tadd.s64 db, %2, %12;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p1;\n\t"
+      "add.u32 ta, %1, 56;\n\tadd.s64 db, %2, %13;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p1;\n\t}\n"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc), "r"(1u),
+      "n"(B0), "n"(B1), "n"(B2), "n"(B3), "n"(B4), "n"(B5), "n"(B6), "n"(B7)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
