@@ -384,7 +384,11 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
       auto issue_scores = [&](int stage) {
         tc_fence_after();
         const uint32_t ks = k0 + stage * L::kTileBytes;
-        if constexpr (!F8 && D == 128) {
+        if constexpr (F8) {
+          // four K = 32 steps, 32 bytes each inside the 128-byte rows
+          mma4_f8_ss<0, 2, 4, 6, 0, 2, 4, 6>(tmem + L::col_s(i), sdesc_sw128(qs, 16, 1024), sdesc_sw128(ks, 16, 1024),
+                                              idesc_s, 0u);
+        } else if constexpr (D == 128) {
           // eight K = 16 steps: 32 bytes inside a 64-element sub-tile, then the next sub-tile
           static_assert(L::kSubBytes == 1024 * 16, "step offsets in 16-byte units");
           mma8_bf16_ss<0, 2, 4, 6, 1024, 1026, 1028, 1030, 0, 2, 4, 6, 1024, 1026, 1028, 1030>(
@@ -393,12 +397,8 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
 #pragma unroll
           for (int k = 0; k < D * L::kElem / 32; ++k) {  // 32 bytes of each row per MMA
             const uint32_t off = (k / 4) * L::kSubBytes + (k % 4) * 32;
-            if constexpr (F8)
-              mma_f8_ss(tmem + L::col_s(i), sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + off, 16, 1024),
-                        idesc_s, k > 0 ? 1u : 0u);
-            else
-              mma_bf16_ss(tmem + L::col_s(i), sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + off, 16, 1024),
-                          idesc_s, k > 0 ? 1u : 0u);
+            mma_bf16_ss(tmem + L::col_s(i), sdesc_sw128(qs + off, 16, 1024), sdesc_sw128(ks + off, 16, 1024), idesc_s,
+                        k > 0 ? 1u : 0u);
           }
         }
       };
@@ -435,16 +435,11 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
           if constexpr (F8) {
             // V^T K-major: 32 keys = 32 bytes per step; P: four keys per TMEM column.  P V on
             // keys [0, 64) while the softmax warps finish keys [64, 128), then the rest.
-#pragma unroll
-            for (int k = 0; k < kTile / 32; ++k) {
-              if (k == kTile / 64) {
-                if (!(ok = mbar_wait(&bar.p_hi[i], n & 1, wc))) break;
-                tc_fence_after();
-              }
-              mma_f8_ts(tmem + L::col_o(i), tmem + L::col_s(i) + k * 8, sdesc_sw128(vs + k * 32, 16, 1024), idesc_o,
-                        (n > 0 || k > 0) ? 1u : 0u);
-            }
-            if (!ok) break;
+            const uint64_t vdesc = sdesc_sw128(vs, 16, 1024);
+            mma2_f8_ts<0, 2>(tmem + L::col_o(i), tmem + L::col_s(i), vdesc, idesc_o, n > 0 ? 1u : 0u);
+            if (!(ok = mbar_wait(&bar.p_hi[i], n & 1, wc))) break;
+            tc_fence_after();
+            mma2_f8_ts<4, 6>(tmem + L::col_o(i), tmem + L::col_s(i) + 16, vdesc, idesc_o, 1u);
           } else {
             // V N-major: 16 keys = 2048 bytes per step; P: two keys (eight per K step) per TMEM column
             mma8_bf16_ts<0, 128, 256, 384, 512, 640, 768, 896>(tmem + L::col_o(i), tmem + L::col_s(i),

@@ -230,30 +230,6 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
   return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem] with 8-bit operands; one thread issues.
-__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem] with 8-bit operands; one thread issues.  A holds four
-// K-elements per 32-bit column (element 4c in the lowest byte), so each K = 32 step
-// advances 8 columns.
-__device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Eight kind::f16 MMAs from shared memory into one accumulator, one K = 16 step each:
 // descriptor k of A (B) is `a` (`b`) plus the compile-time offset Ak (Bk), in the
 // descriptor's 16-byte units.  The first MMA accumulates when `acc` is non-zero, the
@@ -298,6 +274,35 @@ __device__ __forceinline__ void mma8_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       "add.u32 ta, %1, 56;\n\tadd.s64 db, %2, %13;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p1;\n\t}\n"
       ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc), "r"(1u),
       "n"(B0), "n"(B1), "n"(B2), "n"(B3), "n"(B4), "n"(B5), "n"(B6), "n"(B7)
+      : "memory");
+}
+
+// Four kind::f8f6f4 MMAs (E4M3 A and B from shared memory, K = 32 each) into one
+// accumulator, offsets as in mma8_bf16_ss.
+template <uint32_t A0, uint32_t A1, uint32_t A2, uint32_t A3, uint32_t B0, uint32_t B1, uint32_t B2, uint32_t B3>
+__device__ __forceinline__ void mma4_f8_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
+      "add.s64 da, %1, %6;\n\tadd.s64 db, %2, %10;\n\ttcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, p0;\n\t"
+      "add.s64 da, %1, %7;\n\tadd.s64 db, %2, %11;\n\ttcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, p1;\n\t"
+      "add.s64 da, %1, %8;\n\tadd.s64 db, %2, %12;\n\ttcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, p1;\n\t"
+      "add.s64 da, %1, %9;\n\tadd.s64 db, %2, %13;\n\ttcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, p1;\n\t}\n"
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(1u),
+      "n"(A0), "n"(A1), "n"(A2), "n"(A3), "n"(B0), "n"(B1), "n"(B2), "n"(B3)
+      : "memory");
+}
+
+// Two kind::f8f6f4 MMAs with A from tensor memory (four E4M3 K-elements per column, so
+// K = 32 is eight columns): step k reads A at a_tmem + 8k and B at b plus the k-th offset.
+template <uint32_t B0, uint32_t B1>
+__device__ __forceinline__ void mma2_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 db;\n\t.reg .b32 ta;\n\t"
+      "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
+      "add.s64 db, %2, %6;\n\ttcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %3, p0;\n\t"
+      "add.u32 ta, %1, 8;\n\tadd.s64 db, %2, %7;\n\ttcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], db, %3, p1;\n\t}\n"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc), "r"(1u), "n"(B0), "n"(B1)
       : "memory");
 }
 
