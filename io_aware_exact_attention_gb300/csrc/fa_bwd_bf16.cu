@@ -513,7 +513,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // processed, and two P/dS buffers so the next P is written while dK, dQ still read
 // this dS.  The P/dS work (a full 128-key row per thread regardless of d) is split by
 // key halves over both compute warpgroups; each warp drains its 32 x 32 block of dQ
-// and writes its 32 x 32 blocks of dV, dK through one private staging block.
+// and writes its 32 x 32 blocks of dV, dK through one private staging block.  Across
+// items the work overlaps: the next item's first scores go out after this item's last
+// dV, and this item's last dQ drain and its dV, dK epilogue run in the next item's
+// first tile pair, after that P is stored (BERT-sized items of <= 4 tiles: -10%).
 template <int D>
 struct PBwdLayout {
   static_assert(D == 64, "the persistent backward is the d = 64 kernel");
@@ -729,16 +732,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_commit(&bar.s_full);
       };
       KvLenAhead kvl(blockIdx.x, gridDim.x, n_items, a);
+      bool s_ahead = false;  // this item's first scores went out during the previous item
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         const BwdItem w = bwd_item(item, kvl.next(item, a), a);
         if (w.first >= T) continue;
         const int kb = kvu % KB;
         const uint32_t k0 = smem_u32(smKV + kb * 2 * L::kTileBytes), v0 = k0 + L::kTileBytes;
-        if (!(ok = mbar_wait(&bar.kv_full[kb], (kvu / KB) & 1, wc))) break;
-        if (!(ok = mbar_wait(&bar.q_full[git % QS], (git / QS) & 1, wc))) break;
-        issue_scores(git % QS, k0);
+        if (!s_ahead) {
+          if (!(ok = mbar_wait(&bar.kv_full[kb], (kvu / KB) & 1, wc))) break;
+          if (!(ok = mbar_wait(&bar.q_full[git % QS], (git / QS) & 1, wc))) break;
+          issue_scores(git % QS, k0);
+        }
+        s_ahead = false;
         // Per query tile: dP, dV, then the next tile's scores (so the P/dS warps can
-        // move straight on), then dK and dQ.
+        // move straight on; after an item's last dV, the next item's first scores, its
+        // K, V being in the other buffer), then dK and dQ.
         int itl = 0;
         for (int qt = w.first; qt < T; ++itl, ++git) {
           const int qt_next = next_query_tile(qt + 1, w.kt, w.kv_len, a.causal, a.block_mask, T);
@@ -772,6 +780,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (qt_next < T) {
             if (!(ok = mbar_wait(&bar.q_full[(git + 1) % QS], ((git + 1) / QS) & 1, wc))) break;
             issue_scores((git + 1) % QS, k0);
+          } else if (item + static_cast<int>(gridDim.x) < n_items) {
+            // the next item's first scores (its K, V are in the other buffer)
+            const BwdItem wn = bwd_item(item + gridDim.x, kvl.peek(), a);
+            if (wn.first < T) {
+              const int kbn = (kvu + 1) % KB;
+              if (!(ok = mbar_wait(&bar.kv_full[kbn], ((kvu + 1) / KB) & 1, wc))) break;
+              if (!(ok = mbar_wait(&bar.q_full[(git + 1) % QS], ((git + 1) / QS) & 1, wc))) break;
+              issue_scores((git + 1) % QS, smem_u32(smKV + kbn * 2 * L::kTileBytes));
+              s_ahead = true;
+            }
           }
           // dK += dS^T Q_i ; dQ_i = dS K_j
           if (!(ok = mbar_wait(&bar.ds_full, git & 1, wc))) break;
@@ -858,6 +876,65 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const BwdItem w0 = bwd_item(blockIdx.x, kvl.peek(), a);
       load_stats(w0.head, w0.first, lse_c, d_c);
     }
+    // The epilogue of an item: this warp's 32 key rows x 32 columns of dV_j and scale * dK_j
+    // as bf16, staged in its own block (64-byte rows, 64-byte swizzle) and stored by TMA;
+    // key tiles no query sees get zeros.  `have`: the item's MMAs are all done and its
+    // accumulators hold dV_j, dK_j.
+    auto epilogue = [&](bool have, int kt_e, int head_e) {
+      uint32_t wv[16], wk[16];
+      {
+        uint32_t tv[32], tk[32];
+        if (have) {
+          tc_fence_after();
+          tmem_ld32(tmem + lane_off + L::kColDV + 32 * hc, tv);
+          tmem_ld32(tmem + lane_off + L::kColDK + 32 * hc, tk);
+          tc_fence_before();
+          mbar_arrive(&bar.acc_free);  // the accumulators may now be overwritten by the next item
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) tv[i] = tk[i] = 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          wv[i] = pack_bf16x2(__uint_as_float(tv[2 * i]), __uint_as_float(tv[2 * i + 1]));
+          wk[i] = pack_bf16x2(__uint_as_float(tk[2 * i]) * a.scale, __uint_as_float(tk[2 * i + 1]) * a.scale);
+        }
+      }
+      if (lane == 0) bulk_wait_read_all();  // the block's last bulk copy (a dQ reduce) has read it
+      __syncwarp();
+      const uint32_t sv = smem_u32(blk), sk = sv + 2048;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        st_shared_v4(sv + sw64_offset(lane, q), wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
+        st_shared_v4(sk + sw64_offset(lane, q), wk[4 * q], wk[4 * q + 1], wk[4 * q + 2], wk[4 * q + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&tm_dv, blk, 32 * hc, kt_e * kTile + wq * 32, head_e);
+        tma_store_3d(&tm_dk, blk + 2048, 32 * hc, kt_e * kTile + wq * 32, head_e);
+        tma_store_commit();
+      }
+    };
+    // An item's last dQ drain and its epilogue are deferred into the next item's first
+    // tile pair, after its P is stored: the next P then overlaps the item's last dK, dQ.
+    bool epi_pending = false, epi_have = false;
+    int epi_kt = 0, epi_head = 0;
+    auto flush_item = [&]() {
+      if (pending) {
+        if (ok && wait_dkdq(git - 1)) {
+          tc_fence_after();
+          drain_dq(pend_qt, pend_head);
+          tc_fence_before();
+          mbar_arrive(&bar.dq_free);
+        }
+        pending = false;
+      }
+      if (epi_pending) {
+        epilogue(epi_have && ok, epi_kt, epi_head);
+        epi_pending = false;
+      }
+    };
     // Every warp walks every item; an aborted CTA (ok == false) only skips the work.
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       const BwdItem w = bwd_item(item, kvl.next(item, a), a);
@@ -919,6 +996,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mbar_arrive(&bar.dq_free);
           pending = false;
         }
+        if (epi_pending) {
+          epilogue(epi_have, epi_kt, epi_head);
+          epi_pending = false;
+        }
 
         ok = mbar_wait(&bar.dp_full, git & 1, wc);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -953,54 +1034,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       lse_c = lse_x;
       d_c = d_x;
-      // end of the item: its last dK, dQ MMAs (and so all its MMAs) are done
-      if (ok && work && wait_dkdq(git - 1)) {
-        tc_fence_after();
-        if (pending) {
-          drain_dq(pend_qt, pend_head);
-          tc_fence_before();
-          mbar_arrive(&bar.dq_free);
-          pending = false;
-        }
-      }
-      // epilogue: this warp's 32 key rows x 32 columns of dV_j and scale * dK_j as bf16,
-      // staged in its own block (64-byte rows, 64-byte swizzle) and stored by TMA; key
-      // tiles no query sees get zeros
-      uint32_t wv[16], wk[16];
-      {
-        uint32_t tv[32], tk[32];
-        if (ok && work) {
-          tc_fence_after();
-          tmem_ld32(tmem + lane_off + L::kColDV + 32 * hc, tv);
-          tmem_ld32(tmem + lane_off + L::kColDK + 32 * hc, tk);
-          tc_fence_before();
-          mbar_arrive(&bar.acc_free);  // the accumulators may now be overwritten by the next item
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) tv[i] = tk[i] = 0u;
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          wv[i] = pack_bf16x2(__uint_as_float(tv[2 * i]), __uint_as_float(tv[2 * i + 1]));
-          wk[i] = pack_bf16x2(__uint_as_float(tk[2 * i]) * a.scale, __uint_as_float(tk[2 * i + 1]) * a.scale);
-        }
-      }
-      if (lane == 0) bulk_wait_read_all();  // the block's last bulk copy (a dQ reduce) has read it
-      __syncwarp();
-      const uint32_t sv = smem_u32(blk), sk = sv + 2048;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        st_shared_v4(sv + sw64_offset(lane, q), wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
-        st_shared_v4(sk + sw64_offset(lane, q), wk[4 * q], wk[4 * q + 1], wk[4 * q + 2], wk[4 * q + 3]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_3d(&tm_dv, blk, 32 * hc, w.kt * kTile + wq * 32, w.head);
-        tma_store_3d(&tm_dk, blk + 2048, 32 * hc, w.kt * kTile + wq * 32, w.head);
-        tma_store_commit();
+      if (work) {
+        // this item's first tile pair ran the previous item's epilogue; one still pending
+        // here means that pair gave up (ok == false), and it only writes zeros
+        if (epi_pending) flush_item();
+        epi_pending = true;
+        epi_have = ok;
+        epi_kt = w.kt;
+        epi_head = w.head;
+      } else {
+        flush_item();
+        epilogue(false, w.kt, w.head);
       }
     }
+    flush_item();
     if (lane == 0) tma_store_wait_all();
   }
 
