@@ -237,6 +237,13 @@ def make_fp8_inputs(B: int, H: int, N: int, d: int, *, seed: int, scale: float |
     masks, quantized to E4M3 with one power-of-two scale per tensor."""
     raw = make_inputs(B, H, N, d, seed=seed, dtype="fp32", scale=scale, causal=causal,
                       kv_len_range=kv_len_range, block_mask=block_mask, with_dout=False)
+    return fp8_inputs_from(raw)
+
+
+def fp8_inputs_from(raw: AttentionInputs) -> Fp8Inputs:
+    """FP8 inputs holding the float32 Q, K, V of `raw` (shape, masks and scale kept),
+    each quantized to E4M3 with one power-of-two scale per tensor."""
+    B, H, N, d = raw.q.shape
     q8, sq, q = quantize_e4m3(raw.q)
     k8, sk, k = quantize_e4m3(raw.k)
     v8, sv, v = quantize_e4m3(raw.v)
@@ -244,7 +251,8 @@ def make_fp8_inputs(B: int, H: int, N: int, d: int, *, seed: int, scale: float |
     vt8 = np.zeros((B, H, d, ldv), np.uint8)
     vt8[..., :N] = np.swapaxes(v8, 2, 3)
     return Fp8Inputs(q8=q8, k8=k8, vt8=vt8, ldv=ldv, descale_q=sq, descale_k=sk, descale_v=sv, q=q, k=k, v=v,
-                     scale=raw.scale, causal=causal, kv_len=raw.kv_len, block_mask=raw.block_mask, seed=seed)
+                     scale=raw.scale, causal=raw.causal, kv_len=raw.kv_len, block_mask=raw.block_mask,
+                     seed=raw.seed)
 
 
 def workload_fp8_inputs(name: str, *, seed: int | None = None, **override) -> Fp8Inputs:

@@ -7,6 +7,8 @@ every element inside its bound, and a relative Frobenius error of at most 0.05
 over the tensor; LSE is held to its own bound (score products only).  A case whose
 probabilities are all exact in E4M3 (identical keys) is held to bf16 precision.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -112,6 +114,31 @@ def test_fp8_identical_keys_exact_probabilities():
     err = np.abs(o - ref[0])
     assert np.all(err <= 2.0 ** -8 * np.abs(ref[0]) + M.ACC_REL * mean_abs_v + 1e-6), f"max err {err.max():.3g}"
     assert np.allclose(ref[0], np.cumsum(inp.v.astype(np.float64), axis=2) / n_vis[:, None], atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_running_max_jumps_between_key_tiles(causal):
+    # Even query rows get a planted score component that jumps between key tiles
+    # (natural log units 0, +5, +20, +28, -2 for key tiles 0..4).  The FP8 kernel's
+    # offset then stays put within its 8-log2-unit slack (+5, for about 85% of the
+    # rows; the rest move past it), moves with an O rescale (+20, +28) and falls
+    # behind (-2).  Odd rows keep plain scores, so warps mix the cases.  The planted
+    # values go through the same E4M3 quantization as the rest.
+    N, d = 640, 128
+    raw = inputs.make_inputs(1, 2, N, d, seed=951 + int(causal), dtype="fp32", causal=causal, with_dout=False)
+    jump = np.array([0.0, 5.0, 20.0, 28.0, -2.0], np.float32)
+    a = 8.0
+    q, k = raw.q.copy(), raw.k.copy()
+    q[:, :, 0::2, 0] = a
+    q[:, :, 1::2, 0] = 0.0
+    k[:, :, :, 0] = np.repeat(jump, 128)[None, None, :] * np.float32(np.sqrt(d) / a)
+    inp = inputs.fp8_inputs_from(dataclasses.replace(raw, q=q, k=k))
+    # the planted jumps survive quantization: mean planted score per key tile, even rows
+    planted = inp.q[0, 0, 0::2, :1].astype(np.float64) @ inp.k[0, 0, :, :1].T.astype(np.float64) * inp.scale
+    per_tile = planted.reshape(planted.shape[0], 5, 128).mean(axis=(0, 2))
+    assert np.allclose(per_tile, jump, atol=0.5), per_tile
+    o, lse = run(inp)
+    check_all(inp, o, lse)
 
 
 def test_fp8_rejects_bad_arguments():

@@ -3,6 +3,8 @@
 The oracle takes one sequence length for queries and keys; for this non-causal
 operation the query block or the keys are zero-padded to a common length, the padded
 keys masked by the key length, which leaves every real row's result unchanged."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -73,6 +75,26 @@ def test_splitkv_matches_oracle(B, H, Nq, Nk, n_splits, kv):
         empty = [b for b, n in enumerate(kv) if n == 0]
         for b in empty:
             assert np.all(o[b] == 0) and np.all(np.isneginf(lse[b]))
+
+
+@pytest.mark.parametrize("n_splits", [1, 2])
+def test_splitkv_running_max_jumps_between_key_tiles(n_splits):
+    # Even query rows get a planted score component that jumps between key tiles
+    # (natural log units 0, +5, +20, +28, -2 for key tiles 0..4).  A partial pass
+    # hands even and odd key tiles to its two query slots, so each slot's running max
+    # jumps too (0, +20, -2 and +5, +28) and the fast exponentials, the kept offset
+    # and the O rescale all occur, with or without a key split.
+    Nq, Nk, d = 256, 640, 128
+    inp = inputs.make_qk_inputs(1, 2, Nq, Nk, d, seed=961 + n_splits)
+    jump = np.array([0.0, 5.0, 20.0, 28.0, -2.0], np.float32)
+    a = 8.0
+    q, k = inp.q.copy(), inp.k.copy()
+    q[:, :, 0::2, 0] = a
+    q[:, :, 1::2, 0] = 0.0
+    k[:, :, :, 0] = inputs.round_bf16(np.repeat(jump, 128)[None, None, :] * np.float32(np.sqrt(d) / a))
+    inp = dataclasses.replace(inp, q=q, k=k)
+    o, lse = run(inp, n_splits)
+    check(inp, o, lse)
 
 
 def test_splitkv_no_keys():
