@@ -751,9 +751,10 @@ __global__ void __launch_bounds__(FwdLayout<128, 2, true>::kThreads, FwdLayout<1
 // the scores of the next key tile are computed while the softmax of this one runs: the
 // MMA warp issues S_{u+1} as soon as the softmax warps have read S_u out of TMEM.
 // K and V have rings of their own (a K stage is free once its score MMA is done, a V
-// stage once its P V is), and one producer lane streams K ahead of V while another
-// loads Q, so the next scores never wait on a V or Q load.  Q is double-buffered by
-// item; an item's Q buffer is the staging tile of its O.
+// stage once its P V is), each filled by a producer lane of its own, and a third lane
+// loads Q: the next scores never wait on a V or Q load, and a K load never waits for a
+// V stage to be freed (with one lane for both, measured 4-5% slower).  Q is
+// double-buffered by item; an item's Q buffer is the staging tile of its O.
 //
 // The per-item barriers (q_full, q_empty, o_free) count only items with at least one
 // visible key tile, in every role: with items skipped by one role but counted by
@@ -899,35 +900,27 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      // K and V of every (item, key tile) pair, K one pair ahead of V
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      int uk = 0, uv = 0;  // K, V ring uses
+    if (lane == 0 || lane == 2) {
+      // lane 0: K, lane 2: V of every (item, key tile) pair, each through its own ring
+      const bool is_k = lane == 0;
+      tma_prefetch_desc(is_k ? &tm_k : &tm_v);
+      uint64_t* full = is_k ? bar.k_full : bar.v_full;
+      uint64_t* empty = is_k ? bar.k_empty : bar.v_empty;
+      uint8_t* ring = is_k ? smK : smV;
+      const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+      int u = 0;
       bool ok = true;
-      FwdCursor ck = pfwd_cursor_from(0, 0, c, G, n_items, a);
-      FwdCursor cv = ck;
-      while (ok && cv.j >= 0) {
-        while (ok && ck.j >= 0 && uk <= uv + 1) {
-          const int s = uk % S;
-          if (uk >= S && !(ok = mbar_wait(&bar.k_empty[s], ((uk / S) - 1) & 1, wc))) break;
-          mbar_arrive_expect_tx(&bar.k_full[s], L::kTileBytes);
-          tma_load_3d(smK + s * L::kTileBytes, &tm_k, &bar.k_full[s], 0, ck.kt * kTile, ck.w.head);
-          ck = pfwd_cursor_next(ck, c, G, n_items, a);
-          ++uk;
-        }
-        if (!ok) break;
-        const int s = uv % S;
-        if (uv >= S && !(ok = mbar_wait(&bar.v_empty[s], ((uv / S) - 1) & 1, wc))) break;
-        mbar_arrive_expect_tx(&bar.v_full[s], L::kTileBytes);
-        tma_load_3d(smV + s * L::kTileBytes, &tm_v, &bar.v_full[s], 0, cv.kt * kTile, cv.w.head);
-        cv = pfwd_cursor_next(cv, c, G, n_items, a);
-        ++uv;
+      for (FwdCursor cu = pfwd_cursor_from(0, 0, c, G, n_items, a); cu.j >= 0;
+           cu = pfwd_cursor_next(cu, c, G, n_items, a)) {
+        const int s = u % S;
+        if (u >= S && !(ok = mbar_wait(&empty[s], ((u / S) - 1) & 1, wc))) break;
+        mbar_arrive_expect_tx(&full[s], L::kTileBytes);
+        tma_load_3d(ring + s * L::kTileBytes, tm, &full[s], 0, cu.kt * kTile, cu.w.head);
+        ++u;
       }
       if (!ok) {
         // let the loads already issued land before the CTA can exit
-        for (int i = (uk > S ? uk - S : 0); i < uk; ++i) mbar_drain(&bar.k_full[i % S], (i / S) & 1, 100000000ull);
-        for (int i = (uv > S ? uv - S : 0); i < uv; ++i) mbar_drain(&bar.v_full[i % S], (i / S) & 1, 100000000ull);
+        for (int i = (u > S ? u - S : 0); i < u; ++i) mbar_drain(&full[i % S], (i / S) & 1, 100000000ull);
       }
     } else if (lane == 1) {
       // Q of every item with a visible key tile; the k-th goes to buffer k % 2, which
