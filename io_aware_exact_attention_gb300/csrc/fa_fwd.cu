@@ -751,10 +751,12 @@ __global__ void __launch_bounds__(FwdLayout<128, 2, true>::kThreads, FwdLayout<1
 // the scores of the next key tile are computed while the softmax of this one runs: the
 // MMA warp issues S_{u+1} as soon as the softmax warps have read S_u out of TMEM.
 // K and V have rings of their own (a K stage is free once its score MMA is done, a V
-// stage once its P V is), each filled by a producer lane of its own, and a third lane
-// loads Q: the next scores never wait on a V or Q load, and a K load never waits for a
-// V stage to be freed (with one lane for both, measured 4-5% slower).  Q is
-// double-buffered by item; an item's Q buffer is the staging tile of its O.
+// stage once its P V is), filled by two producer lanes that run the same loop, and a
+// third lane loads Q.  The two lanes stay converged, so the load of K for pair u + 1
+// goes out together with V for pair u.  That pacing measured fastest: 4-5% ahead of one
+// lane streaming K two pairs ahead of V, and ahead of K and V loads issued each as soon
+// as its stage is free (separate code paths per lane, or one thread polling all rings).
+// Q is double-buffered by item; an item's Q buffer is the staging tile of its O.
 //
 // The per-item barriers (q_full, q_empty, o_free) count only items with at least one
 // visible key tile, in every role: with items skipped by one role but counted by
@@ -901,7 +903,8 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 || lane == 2) {
-      // lane 0: K, lane 2: V of every (item, key tile) pair, each through its own ring
+      // lane 0: K, lane 2: V of every (item, key tile) pair, each through its own ring;
+      // one loop for both lanes, which keeps them in step (see above)
       const bool is_k = lane == 0;
       tma_prefetch_desc(is_k ? &tm_k : &tm_v);
       uint64_t* full = is_k ? bar.k_full : bar.v_full;
