@@ -5,6 +5,7 @@ library routine); the error model is pinned by a worst case it must cover and
 nearly reach, by the CPU simulation of the kernel's rounding of P staying inside
 it, and by a planted packing mistake that the statistical tolerance must catch.
 """
+import dataclasses
 import math
 
 import numpy as np
@@ -69,6 +70,24 @@ def test_fp8_inputs_layout():
     raw = inputs.make_inputs(2, 3, 200, 128, seed=9, dtype="fp32", causal=True, kv_len_range=(50, 200))
     assert np.array_equal(inp.kv_len, raw.kv_len)
     assert np.abs(inp.k - raw.k).max() <= 2.0 ** -4 * np.abs(raw.k).max()
+
+
+def test_fp8_inputs_from_quantizes_given_draws():
+    # the helper behind make_fp8_inputs: the same result from the same fp32 draws, and
+    # planted values (as the FP8 running-max tests use) quantized like the rest
+    raw = inputs.make_inputs(1, 2, 300, 128, seed=11, dtype="fp32", causal=True, with_dout=False)
+    a = inputs.make_fp8_inputs(1, 2, 300, 128, seed=11, causal=True)
+    b = inputs.fp8_inputs_from(raw)
+    for name in ("q8", "k8", "vt8", "q", "k", "v"):
+        assert np.array_equal(getattr(a, name), getattr(b, name)), name
+    assert (a.descale_q, a.descale_k, a.descale_v, a.ldv, a.causal) == (b.descale_q, b.descale_k, b.descale_v, b.ldv,
+                                                                       b.causal)
+    k = raw.k.copy()
+    k[..., 0] = 40.0
+    c = inputs.fp8_inputs_from(dataclasses.replace(raw, k=k))
+    assert c.descale_k > b.descale_k  # the larger planted column sets the tensor's scale
+    assert np.array_equal(c.k, inputs.e4m3_bits_to_f32(c.k8) * np.float32(c.descale_k))
+    assert np.all(c.k[..., 0] == 40.0)  # 40 = 320 * 2^-3 is exact in E4M3
 
 
 def _head(inp, b, h, rows=None):
