@@ -294,9 +294,9 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap& tm_q, const CUtensor
     // ------------------------------------------------------------ TMA producer
     // lane 0: both query tiles, then the K tiles; lane 1: the V tiles.  K and V stages
     // are released separately (a K tile is done once both score products have read
-    // it, a V tile once both P V products have).  The two lanes run one loop and stay
-    // in step: K of key tile u goes out with V of tile u, which measured as fast as K
-    // one tile further ahead (and faster for FP8).
+    // it, a V tile once both P V products have).  The two lanes run one loop, so their
+    // loads go out in step; starting the K lane's loop one key tile further ahead
+    // measured no faster (and slower for FP8).
     if (lane < 2) {
       const bool is_k = lane == 0;
       if (is_k) {
