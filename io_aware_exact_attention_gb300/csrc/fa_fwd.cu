@@ -970,9 +970,11 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
         ok = mbar_wait_sleep(&bar.q_full[0], 0, wc) && mbar_wait_sleep(&bar.k_full[0], 0, wc);
         if (ok) issue_scores(cur, 0);
       }
-      // The next scores go out as soon as the softmax warps have read these out of TMEM:
-      // before this pair's P V inside an item, after it across items (the next item's Q
-      // may wait for this item's epilogue, which waits for this P V).
+      // The next scores go out as soon as the softmax warps have read these out of TMEM,
+      // before this pair's P V, also when they are the next item's first: that item's Q
+      // buffer is freed by the epilogue two items back, which waits for no later P V.
+      // (Issuing them after the item's last P V instead left each item boundary ~5000
+      // clk longer than a pair: 5% of the GPT-2-shaped forward.)
       auto next_scores = [&](const FwdCursor& cur, const FwdCursor& nxt) -> bool {
         if (nxt.j != cur.j && !mbar_wait_sleep(&bar.q_full[nxt.k & 1], (nxt.k >> 1) & 1, wc)) return false;
         if (!mbar_wait_sleep(&bar.k_full[(u + 1) % S], ((u + 1) / S) & 1, wc)) return false;
@@ -983,7 +985,7 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
       while (ok && cur.j >= 0) {
         const FwdCursor nxt = pfwd_cursor_next(cur, c, G, n_items, a);
         const int s = u % S;
-        if (nxt.j == cur.j && !(ok = next_scores(cur, nxt))) break;
+        if (nxt.j >= 0 && !(ok = next_scores(cur, nxt))) break;
         // O (+)= P V; the first product of an item overwrites the accumulator, which the
         // epilogue of the CTA's previous item with a visible key tile must have read out
         if (!(ok = mbar_wait_sleep(&bar.v_full[s], (u / S) & 1, wc))) break;
@@ -996,7 +998,6 @@ __global__ void __launch_bounds__(PFwdLayout<D>::kThreads, 2)
                       idesc_o, (!cur.first || k > 0) ? 1u : 0u);
         mma_commit(&bar.o_done);
         mma_commit(&bar.v_empty[s]);
-        if (nxt.j >= 0 && nxt.j != cur.j && !(ok = next_scores(cur, nxt))) break;
         cur = nxt;
         ++u;
       }
